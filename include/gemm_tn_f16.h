@@ -1,0 +1,133 @@
+/*
+ * gemm_tn_f16 -- multi-stage pipelined fp16 GEMM D = A * B^T for GB300 (sm_103a).
+ *
+ * The operation is the one computed by the kernel of "cute(9) multistage_gemm"
+ * (code listing and section 11 "性能测试"): A is M x K row-major, B is N x K
+ * row-major, D is M x N row-major, D = A @ B^T.  Here the products are
+ * accumulated in fp32 (in tensor memory) and D is rounded to fp16 once,
+ * round-to-nearest-even.  The page's pipeline -- a kStage ring of shared-memory
+ * tiles filled ahead of the MMA (its sections 4-6) and guarded against
+ * read-after-write and write-after-read hazards ("第 6 课：Shared Memory 布局与
+ * 异步流水", section 3) -- is realised with TMA loads, full/empty mbarrier
+ * pairs and tcgen05.mma issued by one thread.
+ *
+ * All entry points are plain C.  Pointers named D, A, B are DEVICE pointers
+ * on the current CUDA device; `stream` is a cudaStream_t (NULL = legacy
+ * default stream) of that device.  The library allocates no device memory.
+ * Every function returns a gemm_status_t value (0 = success) unless stated.
+ */
+#ifndef GEMM_TN_F16_H
+#define GEMM_TN_F16_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GEMM_OK = 0,
+  GEMM_ERR_INVALID_VALUE = 1,     /* negative or too-large size, NULL pointer, overlap, bad option */
+  GEMM_ERR_MISALIGNED = 2,        /* pointer not 16-byte aligned, or K or N not a multiple of 8 */
+  GEMM_ERR_UNSUPPORTED_DEVICE = 3,/* current device is not compute capability 10.3 */
+  GEMM_ERR_LAUNCH = 4,            /* the kernel launch itself failed */
+  GEMM_ERR_TIMEOUT = 5,           /* a pipeline wait in the kernel gave up (see gemm_get_device_error) */
+  GEMM_ERR_CUDA = 6               /* another CUDA runtime error (no device, memset failed, ...) */
+} gemm_status_t;
+
+/* Kernel paths. */
+enum {
+  GEMM_PATH_AUTO = 0,    /* choose from the shape */
+  GEMM_PATH_SQUARE = 1,  /* persistent 128 x BN tiles, compute-bound shapes */
+  GEMM_PATH_SKINNY = 2   /* M <= 128: one M tile, N spread over every SM, B streamed once */
+};
+
+/*
+ * gemm_tn_f16: D[i][j] = fp16_rn( sum_k A[i][k] * B[j][k] ), fp32 accumulation.
+ *
+ *   D  device, M*N fp16, row-major, leading dimension N.  Written only.
+ *   A  device, M*K fp16, row-major, leading dimension K.  Read only.
+ *   B  device, N*K fp16, row-major, leading dimension K.  Read only.
+ *   M, N, K  0 <= M, N, K <= 2^31 - 1.
+ *
+ * Requirements (checked on the host before anything is launched):
+ *   - A, B, D 16-byte aligned and K % 8 == 0, N % 8 == 0 (TMA strides are
+ *     multiples of 16 bytes), else GEMM_ERR_MISALIGNED;
+ *   - D must not overlap A or B, pointers non-NULL when M*N > 0,
+ *     else GEMM_ERR_INVALID_VALUE;
+ *   - current device of compute capability 10.3, else GEMM_ERR_UNSUPPORTED_DEVICE.
+ * M, N, K need not be multiples of the tile sizes: loads past the edge read
+ * zeros and stores past the edge are clipped.  M == 0 or N == 0 is a no-op;
+ * K == 0 writes D = 0 (the empty sum).
+ * The call is asynchronous on `stream`.  A launch failure returns
+ * GEMM_ERR_LAUNCH; a pipeline wait that times out inside the kernel (no
+ * progress for the timeout, 2 s by default) is reported by
+ * gemm_get_device_error().  The caller owns all buffers.
+ */
+int gemm_tn_f16(void* D, const void* A, const void* B, int64_t M, int64_t N, int64_t K,
+                void* stream);
+
+/* Options for gemm_tn_f16_ex.  Zero-initialise and set what you need. */
+typedef struct {
+  int path;            /* GEMM_PATH_*                                           */
+  int bn;              /* tile width along N: 0 = choose, else 32..256, % 32 == 0 */
+  int kstage;          /* shared-memory ring depth: 0 = deepest that fits, else 2..16 */
+  int max_ctas;        /* persistent CTAs: 0 = one per SM                        */
+  int group_m;         /* m-blocks per rasterisation group: 0 = choose           */
+  uint64_t timeout_ns; /* per-wait limit inside the kernel: 0 = 2 s              */
+  int inject;          /* test hook: 1 = the producer announces its first stage
+                          but never loads it, so the consumers' waits run out;
+                          the kernel then reports GEMM_ERR_TIMEOUT and exits   */
+} gemm_options_t;
+
+/* gemm_tn_f16 with an explicit configuration (sweeps, tests).  Same
+ * arguments, ownership and errors as gemm_tn_f16; an option out of range
+ * returns GEMM_ERR_INVALID_VALUE.  `opt` may be NULL (= all zero). */
+int gemm_tn_f16_ex(void* D, const void* A, const void* B, int64_t M, int64_t N, int64_t K,
+                   const gemm_options_t* opt, void* stream);
+
+/* Chosen configuration for a shape (host only, no GPU work; needs a current
+ * device only to read its SM count -- with no device, 148 SMs are assumed). */
+typedef struct {
+  int path, bm, bn, bk, kstage, ctas, group_m, tiles;
+  int smem_bytes, tmem_cols;
+} gemm_config_t;
+int gemm_query_config(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt,
+                      gemm_config_t* out);
+
+/* Synchronises `stream`, then returns and clears the device error word of the
+ * current device: GEMM_OK, or GEMM_ERR_TIMEOUT if a kernel gave up waiting.
+ * If `raw` is not NULL it receives the raw word (low byte = status, next byte
+ * = the wait site that gave up: 1 producer/empty, 2 mma/full, 3 mma/tmem-empty,
+ * 4 epilogue/tmem-full). */
+int gemm_get_device_error(void* stream, uint32_t* raw);
+
+/* Minimum ring depth that hides a copy latency behind compute:
+ * S_min = ceil(copy_cycles / compute_cycles) + 1 ("第 6 课：Shared Memory 布局与
+ * 异步流水", section 4: in-flight stages >= ceil(T_copy/T_compute), plus the one
+ * being consumed).  Both arguments must be positive; otherwise returns -1.
+ * Host only. */
+int64_t gemm_minimum_stages(int64_t copy_cycles, int64_t compute_cycles);
+
+/* Latency probes on the current device (the two inputs of S_min), in SM clock
+ * cycles, averaged over `reps` measurements each:
+ *   copy_cycles    -- one stage's TMA loads (A 128x64 + B bn x 64 fp16) from
+ *                     issue to the full barrier completing, one stage in
+ *                     flight per SM, `ctas` SMs loading at once (0 = all SMs),
+ *                     addresses strided through a `footprint_bytes` region of
+ *                     `scratch` (device, >= footprint_bytes, caller-owned) so
+ *                     that loads miss L2 when the region exceeds it;
+ *   compute_cycles -- one k-block of MMAs (4 x tcgen05.mma 128 x bn x 16)
+ *                     issued back to back, per k-block.
+ * Synchronous. */
+int gemm_probe_latencies(int bn, int ctas, const void* scratch, int64_t footprint_bytes, int reps,
+                         double* copy_cycles, double* compute_cycles, void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* gemm_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_TN_F16_H */

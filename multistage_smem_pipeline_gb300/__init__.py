@@ -4,14 +4,16 @@ The compute path is the C-ABI library built from ``csrc/`` (TMA + mbarrier
 stage ring + tcgen05/TMEM kernels for sm_103a).  ``binding`` marshals torch
 tensors into that library; it has no fallback of any kind.
 """
-__all__ = ["gemm_tn_f16", "gemm_tn_f16_ex", "get_device_error", "minimum_stages",
-           "query_config", "library_path"]
+_EXPORTS = ("gemm_tn_f16", "gemm_tn_f16_ex", "gemm_tn_f16_from_host", "get_device_error",
+            "minimum_stages", "query_config", "probe_latencies", "library_path", "status_string",
+            "GemmError")
+__all__ = list(_EXPORTS)
 
 
 def __getattr__(name):
     # the CUDA library is loaded on first use, so that importing the package
     # (e.g. for ``synthetic``) works on machines without it
-    if name in __all__:
+    if name in _EXPORTS:
         from . import binding
         return getattr(binding, name)
     raise AttributeError(name)

@@ -1,0 +1,280 @@
+// Persistent, warp-specialised fp16 TN GEMM for sm_103a.
+//
+// One CTA per SM walks a list of 128 x BN output tiles.  Inside the CTA:
+//   warp 0, one thread  -- producer: TMA loads of the A (128 x 64) and B
+//                          (BN x 64) k-blocks into a `stages`-deep ring;
+//   warp 1, one thread  -- MMA issuer: 4 x tcgen05.mma (K = 16 each) per
+//                          k-block into an fp32 accumulator in TMEM;
+//   warps 2-5           -- epilogue: TMEM -> registers -> fp16 -> swizzled
+//                          shared memory -> TMA store, while the MMA thread
+//                          already fills the second TMEM accumulator.
+//
+// This is the multistage pipeline of "cute(9) multistage_gemm" (sections 4-6:
+// a ring of kStage K-tiles, a prologue that runs ahead, a mainloop that
+// overlaps the copy of tile k+S-1 with the MMA of tile k) in Blackwell form.
+// The page's cp_async_wait<kStage-2> + __syncthreads (the read-after-write
+// guard) becomes a wait on the stage's "full" mbarrier, whose transaction
+// count the TMA engine decrements as bytes land; the page's rule that a stage
+// is overwritten only after all its reads (the write-after-read guard,
+// "第 6 课：Shared Memory 布局与异步流水", section 3) becomes the "empty"
+// mbarrier that tcgen05.commit arrives on once the MMAs reading the stage
+// have completed.  The prologue's "fill kStage-1 stages" is implicit: the
+// producer runs ahead until every empty barrier is taken.  The page's
+// register double-buffer (ldmatrix of ik+1 during the MMA of ik) has no
+// counterpart: tcgen05.mma reads its operands from shared memory directly.
+// The page's Reg->Global epilogue is replaced by the Reg->Shared->Global form
+// its section 7 recommends, using TMA stores.
+//
+// Every wait is bounded (a per-wait %globaltimer limit); on expiry the
+// kernel records GEMM_ERR_TIMEOUT in a device error word, all roles leave
+// their loops, in-flight copies and MMAs are drained with bounded waits, and
+// TMEM is freed, so the context stays usable.
+#pragma once
+#include "pipeline.cuh"
+
+namespace gb300 {
+
+__device__ unsigned int g_gemm_error;  // first error of any kernel on this device (0 = none)
+
+__device__ __forceinline__ void record_error(uint32_t code, uint32_t site) {
+  atomicCAS(&g_gemm_error, 0u, code | (site << 8));
+}
+
+// Wait for phase `parity` of `bar`; give up when the CTA is aborting or after
+// timeout_ns without completion (then record the error and start the abort).
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
+                                              volatile int* abort_flag, uint32_t site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 31u) == 0) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > timeout_ns) {
+        *abort_flag = 1;
+        record_error(kErrTimeout, site);
+        return false;
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tn_f16_persistent(const __grid_constant__ CUtensorMap tmA,
+                           const __grid_constant__ CUtensorMap tmB,
+                           const __grid_constant__ CUtensorMap tmD, const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const smem = smem_raw + (base - raw);
+  const SmemLayout L = SmemLayout::make(p.stages, p.stage_bytes);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int S = p.stages;
+  const uint32_t bars = base + L.bars;
+  auto full_bar = [&](int s) { return bars + 8u * s; };
+  auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
+  auto tfull_bar = [&](int b) { return bars + 8u * (2 * S + b); };
+  auto tempty_bar = [&](int b) { return bars + 8u * (2 * S + 2 + b); };
+  const uint32_t drain_bar = bars + 8u * (2 * S + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);   // producer's arrive.expect_tx; TMA bytes complete it
+      mbar_init(empty_bar(s), 1);  // one tcgen05.commit per consumed stage
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);          // tcgen05.commit after a tile's last k-block
+      mbar_init(tempty_bar(b), kEpiWarps); // one arrive per epilogue warp
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmD);
+  }
+  __syncwarp();  // reconverge warp 0 before the aligned CTA barrier
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), p.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol_b = l2_policy_evict_first();
+      const uint64_t pol_a = l2_policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0;
+      for (int t = blockIdx.x; t < p.num_tiles && !*abort_flag; t += gridDim.x) {
+        int mb, nb;
+        tile_coords(t, p, mb, nb);
+        bool ok = true;
+        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+          if (!wait_or_abort(empty_bar(stage), phase ^ 1u, p.timeout_ns, abort_flag, kSiteEmpty)) {
+            ok = false;
+            break;
+          }
+          const uint32_t a_dst = base + L.ring + stage * p.stage_bytes;
+          const uint32_t b_dst = a_dst + kABytes;
+          mbar_arrive_expect_tx(full_bar(stage), p.stage_bytes);
+          if (!(p.inject == 1 && issued == 0)) {
+            if (p.l2_hints & 2u)
+              tma_load_2d_hint(a_dst, &tmA, full_bar(stage), kb * kBK, mb * kBM, pol_a);
+            else
+              tma_load_2d(a_dst, &tmA, full_bar(stage), kb * kBK, mb * kBM);
+            if (p.l2_hints & 1u)
+              tma_load_2d_hint(b_dst, &tmB, full_bar(stage), kb * kBK, nb * p.bn, pol_b);
+            else
+              tma_load_2d(b_dst, &tmB, full_bar(stage), kb * kBK, nb * p.bn);
+          }
+          ++issued;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+      }
+      // Drain: the loads of the last min(issued, S) stages must have landed
+      // before the CTA (and its shared memory) goes away.
+      const uint32_t first = issued > static_cast<uint32_t>(S) ? issued - S : 0u;
+      for (uint32_t i = first; i < issued; ++i)
+        wait_timed(full_bar(i % S), (i / S) & 1u, p.timeout_ns);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+        if (!wait_or_abort(tempty_bar(acc), acc_phase ^ 1u, p.timeout_ns, abort_flag,
+                           kSiteTmemEmpty))
+          break;
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * p.bn);
+        bool ok = true;
+        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+          if (!wait_or_abort(full_bar(stage), phase, p.timeout_ns, abort_flag, kSiteFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t a_src = base + L.ring + stage * p.stage_bytes;
+          const uint64_t a_desc = sw128_kmajor_desc(a_src);
+          const uint64_t b_desc = sw128_kmajor_desc(a_src + kABytes);
+#pragma unroll
+          for (int k = 0; k < kBK / kUmmaK; ++k) {
+            // +32 bytes along K inside the 128-byte swizzle row = +2 in the
+            // descriptor's address field (16-byte units)
+            umma_f16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, p.idesc, (kb | k) != 0);
+          }
+          umma_commit(empty_bar(stage));  // frees the stage once these MMAs have read it
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(tfull_bar(acc));      // accumulator complete
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      // Drain: every MMA issued by this thread completes before TMEM is freed.
+      umma_commit(drain_bar);
+      wait_timed(drain_bar, 0, p.timeout_ns);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const uint32_t my_bufs = base + L.epi + (warp - 2) * kEpiBufs * kEpiChunkBytes;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    uint32_t chunk_seq = 0;
+    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+      int mb, nb;
+      tile_coords(t, p, mb, nb);
+      int ok = 0;
+      if (lane == 0)
+        ok = wait_or_abort(tfull_bar(acc), acc_phase, p.timeout_ns, abort_flag, kSiteTmemFull);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after_sync();
+      const int m0 = mb * kBM + q * 32;
+      const int n0 = nb * p.bn;
+      const bool rows_live = m0 < p.M;
+      const int nchunks = (min(p.bn, p.N - n0) + kEpiCols - 1) / kEpiCols;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(acc * p.bn);
+      for (int c = 0; c < nchunks && rows_live; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(t_row + c * kEpiCols, r);
+        tmem_ld_wait();
+        if (c == nchunks - 1) {  // accumulator fully read: hand it back to the MMA thread
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty_bar(acc));
+        }
+        const uint32_t buf = my_bufs + (chunk_seq % kEpiBufs) * kEpiChunkBytes;
+        if (chunk_seq >= static_cast<uint32_t>(kEpiBufs)) {
+          if (lane == 0) bulk_wait_group_read<kEpiBufs - 1>();  // buffer's last store has read it
+          __syncwarp();
+        }
+        // Row `lane` of the 32 x 32 box, 64 bytes = four 16-byte pieces, placed
+        // with the 64-byte swizzle the TMA store expects (piece j of row r at
+        // position j ^ ((r >> 1) & 3)); conflict-free across the warp.
+        const uint32_t row_addr = buf + lane * 64u;
+        const uint32_t sw = (lane >> 1) & 3u;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          st_shared_v4(row_addr + ((j ^ sw) << 4), pack_half2(r[8 * j + 0], r[8 * j + 1]),
+                       pack_half2(r[8 * j + 2], r[8 * j + 3]),
+                       pack_half2(r[8 * j + 4], r[8 * j + 5]),
+                       pack_half2(r[8 * j + 6], r[8 * j + 7]));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tmD, buf, n0 + c * kEpiCols, m0);
+          bulk_commit_group();
+        }
+        ++chunk_seq;
+      }
+      if (!rows_live) {  // this quadrant lies below M: nothing to store, release at once
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty_bar(acc));
+      }
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if (lane == 0) bulk_wait_group_all();
+    __syncwarp();
+  }
+
+  __syncwarp();  // single-lane roles rejoin their warps
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, p.tmem_cols);
+  }
+}
+
+}  // namespace gb300

@@ -1,0 +1,90 @@
+// Constants, parameter block, shared-memory carve-up and small device helpers
+// shared by the GEMM kernel and the latency probes.
+#pragma once
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace gb300 {
+
+constexpr int kBM = 128;             // UMMA M: one TMEM lane per output row
+constexpr int kBK = 64;              // 64 fp16 = 128 B = one 128-byte swizzle row
+constexpr int kUmmaK = 16;           // K per tcgen05.mma (kind::f16)
+constexpr int kThreads = 192;        // 6 warps
+constexpr int kEpiWarps = 4;
+constexpr int kEpiBufs = 2;          // store staging buffers per epilogue warp
+constexpr int kEpiCols = 32;         // columns per epilogue chunk (one tcgen05.ld x32)
+constexpr uint32_t kEpiChunkBytes = 32 * kEpiCols * 2;  // 32 rows x 32 fp16
+constexpr uint32_t kABytes = kBM * kBK * 2;             // 16 KiB
+constexpr int kMaxStages = 16;
+constexpr uint32_t kErrTimeout = 5;  // == GEMM_ERR_TIMEOUT
+
+enum WaitSite : uint32_t { kSiteEmpty = 1, kSiteFull = 2, kSiteTmemEmpty = 3, kSiteTmemFull = 4 };
+
+struct GemmParams {
+  int32_t M, N, K;
+  int32_t bn;            // tile width along N (multiple of 32, 32..256)
+  int32_t stages;        // ring depth (2..kMaxStages)
+  int32_t num_m_blocks, num_n_blocks, num_k_blocks, num_tiles;
+  int32_t group_m;       // m-blocks per rasterisation group
+  uint32_t idesc;        // tcgen05 instruction descriptor
+  uint32_t tmem_cols;    // allocated TMEM columns (power of two >= 2*bn)
+  uint32_t stage_bytes;  // kABytes + bn * 128
+  uint32_t l2_hints;     // bit 0: stream B with evict-first; bit 1: keep A with evict-last
+  uint64_t timeout_ns;
+  int32_t inject;
+};
+
+// Shared-memory carve-up, offsets from the 1024-aligned base.
+struct SmemLayout {
+  uint32_t ring, epi, bars, misc, total;
+  __host__ __device__ static SmemLayout make(int stages, uint32_t stage_bytes) {
+    SmemLayout L;
+    L.ring = 0;
+    L.epi = stages * stage_bytes;
+    L.bars = L.epi + kEpiWarps * kEpiBufs * kEpiChunkBytes;
+    L.misc = L.bars + 8 * (2 * stages + 5);
+    L.total = L.misc + 16;
+    return L;
+  }
+};
+
+// Bounded wait that ignores the abort flag: used while draining.
+__device__ __forceinline__ bool wait_timed(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 31u) == 0 && global_timer_ns() - t0 > timeout_ns) return false;
+  }
+}
+
+// Grouped rasterisation: consecutive tile ids walk down `group_m` m-blocks
+// before moving to the next n-block, so the tiles in flight at once share
+// their A rows and B rows in L2.
+__device__ __forceinline__ void tile_coords(int t, const GemmParams& p, int& mb, int& nb) {
+  const int group_tiles = p.group_m * p.num_n_blocks;
+  const int g = t / group_tiles;
+  const int first_m = g * p.group_m;
+  const int gm = min(p.num_m_blocks - first_m, p.group_m);
+  const int in = t - g * group_tiles;
+  mb = first_m + in % gm;
+  nb = in / gm;
+}
+
+__device__ __forceinline__ uint32_t pack_half2(uint32_t lo_bits, uint32_t hi_bits) {
+  const __half2 h = __floats2half2_rn(__uint_as_float(lo_bits), __uint_as_float(hi_bits));
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+}  // namespace gb300

@@ -1,0 +1,134 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+include/gemm_tn_f16.h declares, and rejects bad arguments on the host before
+touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import cuda_available
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gemm_tn_f16.h")
+
+
+@pytest.fixture(scope="module")
+def binding():
+    from multistage_smem_pipeline_gb300 import build
+    build.build()
+    from multistage_smem_pipeline_gb300 import binding as b
+    return b
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(gemm_[a-z0-9_]+)\s*\(", text,
+                       flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for want in ("gemm_tn_f16", "gemm_tn_f16_ex", "gemm_get_device_error", "gemm_minimum_stages",
+                 "gemm_query_config", "gemm_probe_latencies", "gemm_status_string"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(binding):
+    lib = ctypes.CDLL(binding.library_path())
+    for name in _declared_functions():
+        assert hasattr(lib, name), f"{name} declared in the header but not exported"
+    assert set(binding.EXPORTED) <= set(_declared_functions())
+
+
+def test_library_is_in_tree_and_built_for_sm103a(binding):
+    path = binding.library_path()
+    assert path.startswith(os.path.join(ROOT, "multistage_smem_pipeline_gb300"))
+    from multistage_smem_pipeline_gb300 import build
+    assert "arch=compute_103a,code=sm_103a" in build.ARCH
+
+
+def test_minimum_stages_matches_page_examples(binding):
+    # same golden rows the oracle is pinned to
+    with open(os.path.join(ROOT, "tests", "golden", "minimum_stages.txt")) as f:
+        rows = [tuple(map(int, l.split())) for l in f if l.strip() and not l.startswith("#")]
+    for copy, compute, want in rows:
+        assert binding.minimum_stages(copy, compute) == want
+    assert binding.minimum_stages(241, 120) == 4
+    assert binding.minimum_stages(0, 5) == -1 and binding.minimum_stages(5, -1) == -1
+    assert binding.minimum_stages(2**62, 1) == 2**62 + 1        # no overflow
+
+
+def _call(binding, D, A, B, M, N, K, opts=None):
+    if opts is None:
+        return binding.LIB.gemm_tn_f16(D, A, B, M, N, K, None)
+    return binding.LIB.gemm_tn_f16_ex(D, A, B, M, N, K, ctypes.byref(opts), None)
+
+
+# fake, never dereferenced device addresses: validation rejects them first
+P0, P1, P2 = 0x10000000, 0x20000000, 0x30000000
+
+
+def test_rejects_bad_sizes(binding):
+    for M, N, K in [(-1, 8, 8), (8, -8, 8), (8, 8, -8), (2**31, 8, 8), (8, 8, 2**40)]:
+        assert _call(binding, P0, P1, P2, M, N, K) == binding.GEMM_ERR_INVALID_VALUE
+
+
+def test_rejects_misalignment(binding):
+    assert _call(binding, P0 + 2, P1, P2, 16, 16, 16) == binding.GEMM_ERR_MISALIGNED
+    assert _call(binding, P0, P1 + 8, P2, 16, 16, 16) == binding.GEMM_ERR_MISALIGNED
+    assert _call(binding, P0, P1, P2, 16, 12, 16) == binding.GEMM_ERR_MISALIGNED   # N % 8
+    assert _call(binding, P0, P1, P2, 16, 16, 20) == binding.GEMM_ERR_MISALIGNED   # K % 8
+
+
+def test_rejects_null_and_overlap(binding):
+    assert _call(binding, 0, P1, P2, 16, 16, 16) == binding.GEMM_ERR_INVALID_VALUE
+    assert _call(binding, P0, 0, P2, 16, 16, 16) == binding.GEMM_ERR_INVALID_VALUE
+    # D = [P1, P1 + 512) overlaps A = [P1 + 256, ...)
+    assert _call(binding, P1, P1 + 256, P2, 16, 16, 16) == binding.GEMM_ERR_INVALID_VALUE
+
+
+def test_empty_output_is_a_noop_without_device(binding):
+    assert _call(binding, 0, 0, 0, 0, 16, 16) == binding.GEMM_OK
+    assert _call(binding, 0, 0, 0, 16, 0, 16) == binding.GEMM_OK
+
+
+def test_rejects_bad_options(binding):
+    for kw in [dict(bn=48), dict(bn=512), dict(kstage=1), dict(kstage=17), dict(path=3),
+               dict(inject=2), dict(max_ctas=-1), dict(path=binding.PATH_SKINNY)]:
+        o = binding._options(**kw)
+        M = 256 if kw.get("path") == binding.PATH_SKINNY else 64
+        assert _call(binding, P0, P1, P2, M, 64, 64, o) == binding.GEMM_ERR_INVALID_VALUE, kw
+
+
+@pytest.mark.skipif(cuda_available(), reason="checks the no-device error path")
+def test_valid_call_without_a_device_reports_cuda_error(binding):
+    assert _call(binding, P0, P1, P2, 64, 64, 64) in (binding.GEMM_ERR_CUDA,
+                                                      binding.GEMM_ERR_UNSUPPORTED_DEVICE)
+
+
+def test_query_config_plans(binding):
+    c = binding.query_config(8192, 8192, 8192)
+    assert c["path"] == binding.PATH_SQUARE and c["bm"] == 128 and c["bk"] == 64
+    assert c["bn"] % 32 == 0 and 32 <= c["bn"] <= 256
+    assert c["kstage"] >= 2 and c["smem_bytes"] <= 232448
+    assert c["tmem_cols"] >= 2 * c["bn"] and c["tmem_cols"] <= 512
+    assert c["tmem_cols"] & (c["tmem_cols"] - 1) == 0
+    s = binding.query_config(128, 14336, 4096)
+    assert s["path"] == binding.PATH_SKINNY and s["tiles"] <= s["ctas"] * 2
+    # every explicit (bn, kstage) that is accepted fits the shared-memory budget
+    for bn in range(32, 257, 32):
+        deepest = binding.query_config(1024, 1024, 1024, bn=bn)["kstage"]
+        for ks in range(2, deepest + 1):
+            cc = binding.query_config(1024, 1024, 1024, bn=bn, kstage=ks)
+            assert cc["smem_bytes"] <= 232448 and cc["kstage"] == ks
+        with pytest.raises(binding.GemmError):
+            binding.query_config(1024, 1024, 1024, bn=bn, kstage=deepest + 1)
+
+
+def test_status_strings(binding):
+    assert binding.status_string(0) == "GEMM_OK"
+    assert binding.status_string(5) == "GEMM_ERR_TIMEOUT"
+    assert binding.status_string(99) == "GEMM_ERR_UNKNOWN"

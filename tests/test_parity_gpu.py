@@ -1,0 +1,203 @@
+"""GPU parity: the CUDA path (called through the C-ABI) against the CPU oracle
+on the same seeded fp16 inputs, element by element.
+
+Shapes span several tiles and ragged tails in M, N and K; the five workload
+configurations are checked in the launch configuration the bench times
+(8192^3 on 4096 seeded samples plus tile-seam points, the rest in full).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from multistage_smem_pipeline_gb300 import synthetic
+from tolerance import compare
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lib(gpu):
+    from multistage_smem_pipeline_gb300 import binding
+    return binding
+
+
+def _dev(bits, gpu):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.float16)).to(gpu)
+
+
+def _run(lib, a_bits, b_bits, gpu, **opts):
+    a, b = _dev(a_bits, gpu), _dev(b_bits, gpu)
+    d = lib.gemm_tn_f16_ex(a, b, **opts) if opts else lib.gemm_tn_f16(a, b)
+    torch.cuda.synchronize()
+    status, raw = lib.get_device_error()
+    assert status == 0, f"device error word {raw:#x}"
+    return d.cpu().numpy().view(np.uint16)
+
+
+def _check(got, a_bits, b_bits, ref=None):
+    K = a_bits.shape[1]
+    if ref is None:
+        ref = oracle.gemm_tn(a_bits, b_bits)
+    st = compare(got, ref, K, a_bits, b_bits)
+    assert st["bad"] == 0, st
+    return st
+
+
+# ----------------------------------------------------------------- shapes and tails
+SHAPES = [
+    (128, 256, 64),      # exactly one tile, one k-block
+    (1, 8, 8),           # smallest legal shape: almost all of the box is out of range
+    (7, 24, 40),         # sub-tile everything, K tail inside one k-block
+    (129, 264, 72),      # one past a tile edge in M, N and K
+    (300, 520, 200),     # several tiles, ragged in all three
+    (256, 256, 256),     # the 256^3 workload's shape
+    (384, 96, 1000),     # K tail of 40 after 15 full k-blocks
+    (64, 4096, 128),     # skinny M, many n tiles
+]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_shapes_with_tails(lib, gpu, M, N, K):
+    a = synthetic.uniform_pm1(M * 7 + 1, (M, K))
+    b = synthetic.uniform_pm1(N * 11 + 2, (N, K))
+    _check(_run(lib, a, b, gpu), a, b)
+
+
+@pytest.mark.parametrize("bn", list(range(32, 257, 32)))
+def test_every_tile_width(lib, gpu, bn):
+    M, N, K = 272, 8 * 83, 328          # 3 m-blocks, ragged n, 6 k-blocks (tail 8)
+    a = synthetic.uniform_pm1(bn, (M, K))
+    b = synthetic.uniform_pm1(bn + 1, (N, K))
+    _check(_run(lib, a, b, gpu, bn=bn), a, b)
+
+
+@pytest.mark.parametrize("bn", [256, 128, 64])
+def test_every_ring_depth_and_wrap(lib, gpu, bn):
+    # K = BK * (kstage +- 1) around every depth: the ring wraps mid-tile and
+    # the phase bits flip at different k-blocks; one CTA walks all tiles so
+    # both TMEM accumulators are reused many times.
+    deepest = lib.query_config(256, 512, 4096, bn=bn)["kstage"]
+    a_full = synthetic.uniform_pm1(5, (256, 64 * (deepest + 2)))
+    b_full = synthetic.uniform_pm1(6, (512, 64 * (deepest + 2)))
+    for ks in range(2, deepest + 1):
+        for kb in (ks - 1, ks, ks + 1):
+            K = 64 * kb
+            a = np.ascontiguousarray(a_full[:, :K])
+            b = np.ascontiguousarray(b_full[:, :K])
+            got = _run(lib, a, b, gpu, bn=bn, kstage=ks, max_ctas=1)
+            _check(got, a, b)
+
+
+@pytest.mark.parametrize("ctas,group_m", [(1, 1), (3, 2), (5, 16), (0, 3)])
+def test_persistent_schedules(lib, gpu, ctas, group_m):
+    M, N, K = 128 * 5 + 17, 256 * 3 + 40, 192
+    a = synthetic.uniform_pm1(ctas + 40, (M, K))
+    b = synthetic.uniform_pm1(group_m + 50, (N, K))
+    _check(_run(lib, a, b, gpu, max_ctas=ctas, group_m=group_m, bn=128), a, b)
+
+
+def test_skinny_path_small(lib, gpu):
+    for M in (1, 16, 100, 128):
+        a = synthetic.gaussian(M, (M, 512))
+        b = synthetic.gaussian(M + 1, (1000, 512), 0.02)
+        _check(_run(lib, a, b, gpu, path=lib.PATH_SKINNY), a, b)
+
+
+# ----------------------------------------------------------------- degenerate sizes
+def test_zero_k_writes_zeros(lib, gpu):
+    a = torch.empty((33, 0), dtype=torch.float16, device=gpu)
+    b = torch.empty((40, 0), dtype=torch.float16, device=gpu)
+    d = torch.full((33, 40), 7.0, dtype=torch.float16, device=gpu)
+    lib.gemm_tn_f16(a, b, out=d)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(d).item() == 0
+
+
+def test_empty_m_or_n_is_noop(lib, gpu):
+    a = torch.ones((0, 64), dtype=torch.float16, device=gpu)
+    b = torch.ones((16, 64), dtype=torch.float16, device=gpu)
+    assert lib.gemm_tn_f16(a, b).shape == (0, 16)
+    b0 = torch.ones((0, 64), dtype=torch.float16, device=gpu)
+    assert lib.gemm_tn_f16(b, b0).shape == (16, 0)
+
+
+def test_misaligned_tensor_is_rejected(lib, gpu):
+    base = torch.zeros(64 * 64 + 1, dtype=torch.float16, device=gpu)
+    a = base[1:].view(64, 64)                 # 2-byte offset
+    b = torch.zeros((64, 64), dtype=torch.float16, device=gpu)
+    with pytest.raises(lib.GemmError) as e:
+        lib.gemm_tn_f16(a, b)
+    assert e.value.status == lib.GEMM_ERR_MISALIGNED
+
+
+def test_large_values_and_overflow(lib, gpu):
+    # sums beyond 65504 become inf on both sides; exact small-int sums stay exact
+    a = np.full((128, 64), np.float16(64.0)).view(np.uint16)
+    b = np.full((256, 64), np.float16(32.0)).view(np.uint16)     # 64 * 2048 = 131072 -> inf
+    got = _run(lib, a, b, gpu)
+    assert np.all(got == 0x7C00)
+
+
+# ----------------------------------------------------------------- the five workloads
+def _workload_check(lib, gpu, tag, sampled=False):
+    a, b, spec = synthetic.workload(tag)
+    got = _run(lib, a, b, gpu)
+    if sampled:
+        rows, cols = synthetic.sample_coords(synthetic.seeds(tag)[2], spec["M"], spec["N"])
+        ref = oracle.gemm_tn_sampled(a, b, rows, cols)
+        st = compare(got[rows, cols], ref, spec["K"], a, b)
+        assert st["bad"] == 0, st
+        # properties that hold at any size: finite everywhere, |D| bounded by K*max|a||b|
+        g = got.view(np.float16)
+        assert np.isfinite(g).all()
+        return st
+    return _check(got, a, b)
+
+
+def test_workload_256(lib, gpu):
+    _workload_check(lib, gpu, "c1")
+
+
+def test_workload_1024_ternary_is_bit_exact(lib, gpu):
+    a, b, spec = synthetic.workload("c2")
+    got = _run(lib, a, b, gpu)
+    ref = oracle.gemm_tn(a, b)
+    assert np.array_equal(got, ref)
+    ai = a.view(np.float16).astype(np.int64)
+    bi = b.view(np.float16).astype(np.int64)
+    assert np.array_equal(ref, (ai @ bi.T).astype(np.float16).view(np.uint16))
+
+
+def test_workload_4096(lib, gpu):
+    st = _workload_check(lib, gpu, "c3")
+    assert st["exact_frac"] > 0.95
+
+
+def test_workload_8192_sampled(lib, gpu):
+    st = _workload_check(lib, gpu, "c4", sampled=True)
+    assert st["n"] >= 4096
+
+
+def test_workload_skinny(lib, gpu):
+    st = _workload_check(lib, gpu, "c5")
+    assert st["exact_frac"] > 0.95
+
+
+def test_host_buffers_end_to_end(lib, gpu):
+    a, b, spec = synthetic.workload("c1")
+    ah = torch.from_numpy(a.view(np.float16)).pin_memory()
+    bh = torch.from_numpy(b.view(np.float16)).pin_memory()
+    d = lib.gemm_tn_f16_from_host(ah, bh)
+    _check(d.numpy().view(np.uint16), a, b)
+
+
+def test_side_stream(lib, gpu):
+    a = synthetic.uniform_pm1(77, (300, 256))
+    b = synthetic.uniform_pm1(78, (264, 256))
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        da, db = _dev(a, gpu), _dev(b, gpu)
+        d = lib.gemm_tn_f16(da, db, stream=s)
+    s.synchronize()
+    _check(d.cpu().numpy().view(np.uint16), a, b)

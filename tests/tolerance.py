@@ -1,0 +1,42 @@
+"""Element-wise comparison of the GPU result with the oracle.
+
+Bound per element (fp32 accumulation vs the oracle's exact-then-round):
+    |D_gpu - D_ref| <= 2e-3 * sqrt(K) * max|A| * max|B| + ulp(D_ref)
+where ulp(r) is the fp16 spacing at |r| (2^(max(e, -14) - 10) for
+2^e <= |r| < 2^(e+1)).  The first term bounds the fp32 rounding of K
+accumulated products with room to spare (each product is exact in fp32; the
+running sum rounds at 2^-24 relative), the second the two sides rounding to
+fp16 on either side of a tie.  Integer-valued inputs whose partial sums stay
+exact in fp32 ({-1, 0, 1} at K = 1024) must match bit for bit instead.
+"""
+import numpy as np
+
+
+def fp16_ulp(r: np.ndarray) -> np.ndarray:
+    a = np.abs(r.astype(np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -14)))
+    return np.exp2(e - 10)
+
+
+def tolerance(ref_bits: np.ndarray, K: int, amax: float, bmax: float) -> np.ndarray:
+    r = ref_bits.view(np.float16).astype(np.float64)
+    return 2e-3 * np.sqrt(max(K, 1)) * amax * bmax + fp16_ulp(r)
+
+
+def compare(got_bits: np.ndarray, ref_bits: np.ndarray, K: int, a_bits: np.ndarray,
+            b_bits: np.ndarray) -> dict:
+    """Returns stats; 'bad' counts elements outside the bound (NaN-aware)."""
+    g = got_bits.view(np.float16).astype(np.float64)
+    r = ref_bits.view(np.float16).astype(np.float64)
+    amax = float(np.abs(a_bits.view(np.float16).astype(np.float64)).max()) if a_bits.size else 0.0
+    bmax = float(np.abs(b_bits.view(np.float16).astype(np.float64)).max()) if b_bits.size else 0.0
+    tol = tolerance(ref_bits, K, amax, bmax)
+    both_nan = np.isnan(g) & np.isnan(r)
+    err = np.where(both_nan, 0.0, np.abs(g - r))
+    err = np.where(np.isnan(err), np.inf, err)
+    bad = int(np.count_nonzero(err > tol))
+    ulps = np.abs(got_bits.astype(np.int64) - ref_bits.astype(np.int64))
+    return {"bad": bad, "max_err": float(err.max()) if err.size else 0.0,
+            "max_ulps": int(ulps.max()) if ulps.size else 0,
+            "exact_frac": float(np.mean(got_bits == ref_bits)) if got_bits.size else 1.0,
+            "n": int(got_bits.size)}

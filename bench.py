@@ -1,0 +1,375 @@
+"""Benchmark of gemm_tn_f16 on GB300: one JSON line on stdout (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c1..c5] [--impl reference]
+
+A step is one gemm_tn_f16 call (the whole path: one persistent kernel) on
+seeded synthetic fp16 inputs already resident in HBM.  Before every timed
+launch the L2 is flushed by writing a buffer twice the L2 size; each launch
+is bracketed by CUDA events on its stream and ms_per_step is the mean launch
+time.  Default workload: 8192 x 8192 x 8192, U[-1, 1] operands.
+
+Extra keys: roofline (the GEMM kernel against the measured dense bf16 peak,
+fp16 running at the same nominal rate, or against measured HBM bandwidth for
+the skinny case), cpu_baseline (the CPU oracle timed on a bounded row slice
+of the same workload on this host), e2e (host buffers: H2D of A and B, the
+GEMM, D2H of D, per step), clocks (nvidia-smi sampled during the timed
+region), gpu_launches.
+
+--impl reference times the CPU oracle itself (the only other implementation
+of this computation here) on the same workload and metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from multistage_smem_pipeline_gb300 import synthetic  # noqa: E402
+
+METRIC = "fp16 GEMM TFLOP/s at 8192³ and % of dense FP16 tensor peak (1 GB300)"
+UNIT = "TFLOP/s"
+KERNEL = "gemm_tn_f16_persistent"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def _env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "multistage_smem_pipeline_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from a committed ncu capture, if it was taken on
+    the kernel sources as they are now; otherwise None."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("source_hash") != source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clocks
+CLOCK_FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+                "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+                "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+
+class ClockSampler:
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + ",".join(CLOCK_FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self._t.join(timeout=5)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != len(CLOCK_FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_rate(a_bits, b_bits, target_s: float):
+    """Time the oracle on a slice of rows of A sized to about target_s seconds
+    of wall time on this host.  Returns (flop/s, rows, threads, seconds)."""
+    import oracle
+    threads = oracle.default_threads()
+    K = a_bits.shape[1]
+    N = b_bits.shape[0]
+    t0 = time.perf_counter()
+    oracle.gemm_tn(a_bits[:1], b_bits, threads=1)
+    one_row = max(time.perf_counter() - t0, 1e-6)             # seconds for one row, 1 thread
+    rows = int(max(1, min(a_bits.shape[0], round(target_s / one_row) * threads)))
+    rows = max(threads, (rows // threads) * threads) if rows >= threads else rows
+    rows = min(rows, a_bits.shape[0])
+    t0 = time.perf_counter()
+    oracle.gemm_tn(np.ascontiguousarray(a_bits[:rows]), b_bits, threads=threads)
+    dt = time.perf_counter() - t0
+    return 2.0 * rows * N * K / dt, rows, min(threads, rows), dt
+
+
+def run_reference(args, tag):
+    rank = _env_int("RANK", 0)
+    if rank != 0:
+        return 0
+    import oracle
+    spec = synthetic.WORKLOADS[tag]
+    a_bits, b_bits, _ = synthetic.workload(tag)
+    threads = oracle.default_threads()
+    K = spec["K"]
+    # size one step (a block of D: `threads` rows x `cols` columns) so that the
+    # whole run stays near args.reference_budget seconds of wall time
+    probe_cols = min(256, spec["N"])
+    t0 = time.perf_counter()
+    oracle.gemm_tn(a_bits[:1], np.ascontiguousarray(b_bits[:probe_cols]), threads=1)
+    per_elem = max(time.perf_counter() - t0, 1e-9) / probe_cols
+    budget = max(0.05, args.reference_budget / max(1, args.steps + args.warmup))
+    rows = min(spec["M"], threads)
+    cols = int(min(spec["N"], max(8, budget * min(threads, rows) / per_elem / rows)))
+    a_slice = np.ascontiguousarray(a_bits[:rows])
+    b_slice = np.ascontiguousarray(b_bits[:cols])
+    for _ in range(args.warmup):
+        oracle.gemm_tn(a_slice, b_slice, threads=threads)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.gemm_tn(a_slice, b_slice, threads=threads)
+        times.append(time.perf_counter() - t0)
+    flops = 2.0 * rows * cols * K
+    ms = statistics.mean(times) * 1e3
+    value = flops / (ms * 1e-3) / 1e12
+    sample = (f"a {rows} x {cols} block of D (of {spec['M']} x {spec['N']}, K={K}) per step, "
+              f"full oracle (double accumulation, one fp16 rounding)")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(tag, spec),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": min(threads, rows),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def workload_config(tag, spec, extra=None):
+    c = {"workload": synthetic.WORKLOAD_NAMES[tag], "M": spec["M"], "N": spec["N"],
+         "K": spec["K"], "layout": "TN: A MxK, B NxK row-major, D MxN row-major",
+         "accumulate": "fp32", "output": "fp16", "parallelism": "replicas (one GEMM per GPU)"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_gpu(args, tag):
+    import torch
+    import torch.distributed as dist
+
+    from multistage_smem_pipeline_gb300 import binding
+
+    rank, world, local = _env_int("RANK", 0), _env_int("WORLD_SIZE", 1), _env_int("LOCAL_RANK", 0)
+    if world > 1:
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("gloo", rank=rank, world_size=world)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    spec = synthetic.WORKLOADS[tag]
+    M, N, K = spec["M"], spec["N"], spec["K"]
+    flops = 2.0 * M * N * K
+    alg_bytes = 2.0 * (M * K + N * K + M * N)
+
+    a_bits, b_bits, _ = synthetic.workload(tag)
+    a_host = torch.from_numpy(a_bits.view(np.float16)).pin_memory()
+    b_host = torch.from_numpy(b_bits.view(np.float16)).pin_memory()
+    a = a_host.to(dev)
+    b = b_host.to(dev)
+    d = torch.empty((M, N), dtype=torch.float16, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    cfg = binding.query_config(M, N, K)
+
+    for _ in range(args.warmup):
+        binding.gemm_tn_f16(a, b, out=d, stream=stream)
+    torch.cuda.synchronize(dev)
+    status, raw = binding.get_device_error(stream)
+    if status != 0:
+        raise SystemExit(f"device error after warm-up: {raw:#x}")
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()                           # evict A, B, D from L2 (not timed)
+        starts[i].record(stream)
+        binding.gemm_tn_f16(a, b, out=d, stream=stream)
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    launches_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = statistics.mean(launches_ms)
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    status, raw = binding.get_device_error(stream)
+    if status != 0:
+        raise SystemExit(f"device error in timed region: {raw:#x}")
+
+    # end to end from pinned host buffers through the public API
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    d_host = torch.empty((M, N), dtype=torch.float16, pin_memory=True)
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    e_start.record(stream)
+    for _ in range(e2e_steps):
+        a_e = a_host.to(dev, non_blocking=True)
+        b_e = b_host.to(dev, non_blocking=True)
+        binding.gemm_tn_f16(a_e, b_e, out=d, stream=stream)
+        d_host.copy_(d, non_blocking=True)
+    e_end.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e_start.elapsed_time(e_end) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    if rank != 0:
+        return 0
+
+    peaks, peak_src = load_peaks()
+    tflops = flops / (ms * 1e-3) / 1e12
+    hbm_bound = tag == "c5"
+    if hbm_bound:
+        achieved = alg_bytes / (ms * 1e-3) / 1e9
+        peak = float(peaks["hbm_gbs"])
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "peak_source": f"{peak_src} hbm_gbs (copy bandwidth)"}
+    else:
+        peak = float(peaks["bf16_tflops"])
+        roof = {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                "frac": tflops / peak,
+                "peak_source": f"{peak_src} bf16_tflops (burst) x fp16:bf16 nominal rate 1:1"}
+    roof["kernel"] = KERNEL
+    roof["traffic"] = recorded_traffic(tag)
+    roof["alg_bytes_per_launch"] = alg_bytes
+    roof["flops_per_launch"] = flops
+
+    line = {"metric": METRIC, "value": tflops * world, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+            "data": "synthetic (seeded splitmix64, fp16-rounded)",
+            "config": workload_config(tag, spec, {
+                "l2": "flushed before every timed launch (2 x L2 bytes written, outside the "
+                      "launch's event pair)",
+                "path": ["auto", "square", "skinny"][cfg["path"]], "bm": cfg["bm"],
+                "bn": cfg["bn"], "bk": cfg["bk"], "kstage": cfg["kstage"], "ctas": cfg["ctas"],
+                "tiles": cfg["tiles"]}),
+            "launch_ms": {"mean": ms, "median": statistics.median(launches_ms),
+                          "p10": float(np.percentile(launches_ms, 10)),
+                          "p90": float(np.percentile(launches_ms, 90))},
+            "roofline": roof,
+            "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                    "h2d_bytes_per_step": 2 * (M * K + N * K), "d2h_bytes_per_step": 2 * M * N,
+                    "ms_per_step": e2e_ms, "steps": e2e_steps},
+            "gpu_launches": args.steps,
+            "clocks": clk,
+            "wall_s_timed_region": wall}
+    if world == 1 and not args.no_cpu:
+        rate, rows, cores, dt = oracle_rate(a_bits, b_bits, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": rate / 1e12, "unit": UNIT, "cores": cores,
+                                "kind": "oracle",
+                                "sample": f"{rows} rows of D ({rows}x{N}, K={K}) in {dt:.1f} s; "
+                                          f"full oracle: double accumulation, one fp16 rounding"}
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(synthetic.WORKLOADS), default="c4")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--reference-budget", type=float, default=90.0,
+                    help="target wall seconds for the whole --impl reference run")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        return run_reference(args, args.workload)
+    return run_gpu(args, args.workload)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

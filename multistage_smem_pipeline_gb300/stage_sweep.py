@@ -1,0 +1,86 @@
+"""Ring-depth (kStage) justification on the current GPU.
+
+    python -m multistage_smem_pipeline_gb300.stage_sweep [--workload c4] [--bn 256 128]
+
+1. Measures the two inputs of the stage-count rule of "第 6 课：Shared Memory
+   布局与异步流水" (section 4), S_min = ceil(T_copy / T_compute) + 1, with the
+   library's latency probes: T_copy = one stage's TMA loads (A 128 x 64 and
+   B bn x 64 fp16) from issue to the full barrier, with every SM loading at
+   once, from a region far larger than L2 (HBM) and from one that fits in L2;
+   T_compute = one k-block (4 x tcgen05.mma 128 x bn x 16) on one SM.
+2. Sweeps kstage from 2 to the deepest ring that fits in shared memory for
+   each tile width on the chosen workload, timing each like bench.py.
+3. Prints one JSON object per measurement and a summary line.
+
+Shared memory per CTA: kstage * (16 KiB + bn * 128 B) + 16 KiB of epilogue
+staging; one CTA per SM (persistent), so the page's occupancy collapse
+(fewer resident blocks as stages grow) does not arise -- the only cost of a
+deeper ring is shared memory the kernel does not otherwise use.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+
+import numpy as np
+import torch
+
+from . import binding, synthetic
+from .timing import time_launches
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--workload", default="c4", choices=sorted(synthetic.WORKLOADS))
+    ap.add_argument("--bn", type=int, nargs="+", default=[256, 128])
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--reps", type=int, default=256)
+    args = ap.parse_args()
+
+    dev = torch.device("cuda", 0)
+    spec = synthetic.WORKLOADS[args.workload]
+    M, N, K = spec["M"], spec["N"], spec["K"]
+    a_bits, b_bits, _ = synthetic.workload(args.workload)
+    a = torch.from_numpy(a_bits.view(np.float16)).to(dev)
+    b = torch.from_numpy(b_bits.view(np.float16)).to(dev)
+    d = torch.empty((M, N), dtype=torch.float16, device=dev)
+    flops = 2.0 * M * N * K
+    summary = {}
+    for bn in args.bn:
+        copy_hbm, comp = binding.probe_latencies(bn=bn, ctas=0, footprint_bytes=4 << 30,
+                                                 reps=args.reps // 4)
+        copy_l2, _ = binding.probe_latencies(bn=bn, ctas=0, footprint_bytes=32 << 20,
+                                             reps=args.reps // 4)
+        copy_1sm, comp2 = binding.probe_latencies(bn=bn, ctas=1, footprint_bytes=4 << 30,
+                                                  reps=args.reps)
+        s_hbm = binding.minimum_stages(math.ceil(copy_hbm), math.ceil(comp))
+        s_l2 = binding.minimum_stages(math.ceil(copy_l2), math.ceil(comp))
+        probe = {"kind": "probe", "bn": bn, "t_copy_cycles_all_sms_hbm": copy_hbm,
+                 "t_copy_cycles_all_sms_l2": copy_l2, "t_copy_cycles_one_sm_hbm": copy_1sm,
+                 "t_compute_cycles": comp, "t_compute_cycles_repeat": comp2,
+                 "s_min_hbm": s_hbm, "s_min_l2": s_l2,
+                 "stage_bytes": 16384 + bn * 128}
+        print(json.dumps(probe), flush=True)
+        deepest = binding.query_config(M, N, K, bn=bn)["kstage"]
+        best = None
+        for ks in range(2, deepest + 1):
+            t = time_launches(lambda: binding.gemm_tn_f16_ex(a, b, out=d, bn=bn, kstage=ks),
+                              args.steps, args.warmup, dev)
+            tf = flops / (t["mean"] * 1e-3) / 1e12
+            row = {"kind": "sweep", "workload": args.workload, "bn": bn, "kstage": ks,
+                   "smem_bytes": binding.query_config(M, N, K, bn=bn, kstage=ks)["smem_bytes"],
+                   "ms_mean": t["mean"], "ms_median": t["median"], "tflops": tf}
+            print(json.dumps(row), flush=True)
+            if best is None or tf > best[1]:
+                best = (ks, tf)
+        summary[bn] = {"s_min_hbm": s_hbm, "s_min_l2": s_l2, "deepest": deepest,
+                       "best_kstage": best[0], "best_tflops": best[1]}
+    status, raw = binding.get_device_error()
+    print(json.dumps({"kind": "summary", "workload": args.workload, "per_bn": summary,
+                      "device_status": status}))
+
+
+if __name__ == "__main__":
+    main()

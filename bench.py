@@ -241,10 +241,18 @@ def run_gpu(args, tag):
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    cfg = binding.query_config(M, N, K)
+    opts = {"path": ["auto", "square", "skinny", "pair"].index(args.path), "bn": args.bn,
+            "kstage": args.kstage}
+    forced = any(opts.values())
+    cfg = binding.query_config(M, N, K, **opts)
+
+    def gemm(a_, b_):
+        if forced:
+            return binding.gemm_tn_f16_ex(a_, b_, out=d, stream=stream, **opts)
+        return binding.gemm_tn_f16(a_, b_, out=d, stream=stream)
 
     for _ in range(args.warmup):
-        binding.gemm_tn_f16(a, b, out=d, stream=stream)
+        gemm(a, b)
     torch.cuda.synchronize(dev)
     status, raw = binding.get_device_error(stream)
     if status != 0:
@@ -261,7 +269,7 @@ def run_gpu(args, tag):
     for i in range(args.steps):
         flush.zero_()                           # evict A, B, D from L2 (not timed)
         starts[i].record(stream)
-        binding.gemm_tn_f16(a, b, out=d, stream=stream)
+        gemm(a, b)
         ends[i].record(stream)
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
@@ -290,7 +298,7 @@ def run_gpu(args, tag):
     for _ in range(e2e_steps):
         a_e = a_host.to(dev, non_blocking=True)
         b_e = b_host.to(dev, non_blocking=True)
-        binding.gemm_tn_f16(a_e, b_e, out=d, stream=stream)
+        gemm(a_e, b_e)
         d_host.copy_(d, non_blocking=True)
     e_end.record(stream)
     torch.cuda.synchronize(dev)
@@ -328,9 +336,9 @@ def run_gpu(args, tag):
             "config": workload_config(tag, spec, {
                 "l2": "flushed before every timed launch (2 x L2 bytes written, outside the "
                       "launch's event pair)",
-                "path": ["auto", "square", "skinny"][cfg["path"]], "bm": cfg["bm"],
+                "path": ["auto", "square", "skinny", "pair"][cfg["path"]], "bm": cfg["bm"],
                 "bn": cfg["bn"], "bk": cfg["bk"], "kstage": cfg["kstage"], "ctas": cfg["ctas"],
-                "tiles": cfg["tiles"]}),
+                "tiles": cfg["tiles"], "forced": forced}),
             "launch_ms": {"mean": ms, "median": statistics.median(launches_ms),
                           "p10": float(np.percentile(launches_ms, 10)),
                           "p90": float(np.percentile(launches_ms, 90))},
@@ -363,6 +371,10 @@ def main():
     ap.add_argument("--reference-budget", type=float, default=90.0,
                     help="target wall seconds for the whole --impl reference run")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--path", choices=["auto", "square", "skinny", "pair"], default="auto",
+                    help="diagnostics: force a kernel path (default: the library's choice)")
+    ap.add_argument("--bn", type=int, default=0, help="diagnostics: force the tile width")
+    ap.add_argument("--kstage", type=int, default=0, help="diagnostics: force the ring depth")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

@@ -39,7 +39,8 @@ typedef enum {
 enum {
   GEMM_PATH_AUTO = 0,    /* choose from the shape */
   GEMM_PATH_SQUARE = 1,  /* persistent 128 x BN tiles, compute-bound shapes */
-  GEMM_PATH_SKINNY = 2   /* M <= 128: one M tile, N spread over every SM, B streamed once */
+  GEMM_PATH_SKINNY = 2,  /* M <= 128: one M tile, N spread over every SM, B streamed once */
+  GEMM_PATH_PAIR = 3     /* persistent 256 x BN tiles over CTA pairs (tcgen05 cta_group::2) */
 };
 
 /*
@@ -70,7 +71,8 @@ int gemm_tn_f16(void* D, const void* A, const void* B, int64_t M, int64_t N, int
 /* Options for gemm_tn_f16_ex.  Zero-initialise and set what you need. */
 typedef struct {
   int path;            /* GEMM_PATH_*                                           */
-  int bn;              /* tile width along N: 0 = choose, else 32..256, % 32 == 0 */
+  int bn;              /* tile width along N: 0 = choose, else 32..256, % 32 == 0
+                          (GEMM_PATH_PAIR: the pair's width; each CTA loads bn/2 rows of B) */
   int kstage;          /* shared-memory ring depth: 0 = deepest that fits, else 2..16 */
   int max_ctas;        /* persistent CTAs: 0 = one per SM                        */
   int group_m;         /* m-blocks per rasterisation group: 0 = choose           */

@@ -21,7 +21,7 @@ GEMM_ERR_LAUNCH = 4
 GEMM_ERR_TIMEOUT = 5
 GEMM_ERR_CUDA = 6
 
-PATH_AUTO, PATH_SQUARE, PATH_SKINNY = 0, 1, 2
+PATH_AUTO, PATH_SQUARE, PATH_SKINNY, PATH_PAIR = 0, 1, 2, 3
 
 EXPORTED = ("gemm_tn_f16", "gemm_tn_f16_ex", "gemm_query_config", "gemm_get_device_error",
             "gemm_minimum_stages", "gemm_probe_latencies", "gemm_status_string")

@@ -1,0 +1,257 @@
+// Persistent fp16 TN GEMM over CTA pairs (cluster of 2, tcgen05 cta_group::2).
+//
+// A pair owns a 256 x BN output tile.  Each CTA loads its own 128 rows of A
+// and its own half (BN/2 rows) of B for every k-block into its stage ring;
+// one thread of the even CTA issues tcgen05.mma.cta_group::2 with M = 256,
+// which reads A from each CTA's shared memory and the two halves of B from
+// both, and accumulates each CTA's 128 x BN block of D in that CTA's TMEM.
+// Per SM, a k-block then costs 16 KiB of A + BN/2 x 128 B of B for
+// 128 x BN x 64 MACs -- half the B bytes of a single-CTA tile of the same
+// width -- so a stage is 32 KiB at BN = 256 and six stages fit, which covers
+// the copy latency measured with all SMs loading (S_min = ceil(T_copy /
+// T_compute) + 1 of "第 6 课：Shared Memory 布局与异步流水", section 4).
+//
+// Barriers (same shared-memory offsets in both CTAs):
+//   full[s]      even CTA only, count 1: the even CTA's producer arrives
+//                expecting both CTAs' bytes; both CTAs' TMA loads complete
+//                them (the odd CTA's bytes may land first: the transaction
+//                count may go below zero within a phase, and the phase cannot
+//                complete before the even CTA's arrival).  The odd CTA makes
+//                no remote arrive here: a release at cluster scope per k-block
+//                would put a fence in the producer's loop;
+//   empty[s]     both CTAs, count 1: the pair MMA's commit, multicast;
+//   tfull[b]     both CTAs, count 1: commit after a tile's last k-block, multicast;
+//   tempty[b]    even CTA only, count 8: every epilogue warp of both CTAs;
+//   drain        even CTA: final commit before TMEM is freed.
+// As in the single-CTA kernel, every wait is bounded and a timeout is
+// reported through the device error word.  On that path the odd CTA cannot
+// observe its own loads landing (they complete on the even CTA's barrier);
+// the even CTA's bounded drain of the full barriers, which count both CTAs'
+// bytes, plus the final cluster barrier cover them.
+#pragma once
+#include "gemm_kernel.cuh"
+
+namespace gb300 {
+
+constexpr int kPairEpiArrivals = 2 * kEpiWarps;
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tn_f16_pair(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmD, const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const smem = smem_raw + (base - raw);
+  const SmemLayout L = SmemLayout::make(p.stages, p.stage_bytes);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int S = p.stages;
+  const uint32_t rank = cluster_ctarank();  // 0 = even CTA (issues the MMAs), 1 = odd
+  const int pair = blockIdx.x >> 1;
+  const int num_pairs = gridDim.x >> 1;
+  const int half_bn = p.bn >> 1;
+  const uint32_t bars = base + L.bars;
+  auto full_bar = [&](int s) { return bars + 8u * s; };
+  auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
+  auto tfull_bar = [&](int b) { return bars + 8u * (2 * S + b); };
+  auto tempty_bar = [&](int b) { return bars + 8u * (2 * S + 2 + b); };
+  const uint32_t drain_bar = bars + 8u * (2 * S + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), kPairEpiArrivals);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmD);
+  }
+  __syncwarp();
+  // Both CTAs' barriers exist before any remote arrive or multicast commit,
+  // and the peer is known to be running before the collective TMEM allocation.
+  cluster_sync();
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), p.tmem_cols);  // one warp in each CTA of the pair
+    tmem_relinquish_pair();
+  }
+  tc_fence_before_sync();
+  cluster_sync();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer (both CTAs)
+    if (lane == 0) {
+      const uint64_t pol_a = l2_policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0;
+      for (int t = pair; t < p.num_tiles && !*abort_flag; t += num_pairs) {
+        int mb, nb;
+        tile_coords(t, p, mb, nb);           // mb counts 256-row pair blocks
+        const int a_row = mb * (2 * kBM) + static_cast<int>(rank) * kBM;
+        const int b_row = nb * p.bn + static_cast<int>(rank) * half_bn;
+        bool ok = true;
+        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+          if (!wait_or_abort(empty_bar(stage), phase ^ 1u, p.timeout_ns, abort_flag, kSiteEmpty)) {
+            ok = false;
+            break;
+          }
+          const uint32_t a_dst = base + L.ring + stage * p.stage_bytes;
+          const uint32_t b_dst = a_dst + kABytes;
+          const uint32_t leader_full = mapa_shared(full_bar(stage), 0);
+          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2u * p.stage_bytes);
+          if (!(p.inject == 1 && issued == 0 && rank == 0)) {
+            if (p.l2_hints & 2u)
+              tma_load_2d_pair_hint(a_dst, &tmA, leader_full, kb * kBK, a_row, pol_a);
+            else
+              tma_load_2d_pair(a_dst, &tmA, leader_full, kb * kBK, a_row);
+            tma_load_2d_pair(b_dst, &tmB, leader_full, kb * kBK, b_row);
+          }
+          ++issued;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+      }
+      if (rank == 0) {  // the even CTA's full barriers count both CTAs' bytes
+        const uint32_t first = issued > static_cast<uint32_t>(S) ? issued - S : 0u;
+        for (uint32_t i = first; i < issued; ++i)
+          wait_timed(full_bar(i % S), (i / S) & 1u, p.timeout_ns);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (lane == 0 && rank == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      for (int t = pair; t < p.num_tiles; t += num_pairs) {
+        if (!wait_or_abort(tempty_bar(acc), acc_phase ^ 1u, p.timeout_ns, abort_flag,
+                           kSiteTmemEmpty))
+          break;
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * p.bn);
+        bool ok = true;
+        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+          if (!wait_or_abort(full_bar(stage), phase, p.timeout_ns, abort_flag, kSiteFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t a_src = base + L.ring + stage * p.stage_bytes;
+          const uint64_t a_desc = sw128_kmajor_desc(a_src);
+          const uint64_t b_desc = sw128_kmajor_desc(a_src + kABytes);
+#pragma unroll
+          for (int k = 0; k < kBK / kUmmaK; ++k)
+            umma_f16_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, p.idesc, (kb | k) != 0);
+          umma_commit_pair_mc(empty_bar(stage), 0x3);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit_pair_mc(tfull_bar(acc), 0x3);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      umma_commit_pair_mc(drain_bar, 0x1);
+      wait_timed(drain_bar, 0, p.timeout_ns);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;
+    const uint32_t my_bufs = base + L.epi + (warp - 2) * kEpiBufs * kEpiChunkBytes;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    uint32_t chunk_seq = 0;
+    for (int t = pair; t < p.num_tiles; t += num_pairs) {
+      int mb, nb;
+      tile_coords(t, p, mb, nb);
+      int ok = 0;
+      if (lane == 0)
+        ok = wait_or_abort(tfull_bar(acc), acc_phase, p.timeout_ns, abort_flag, kSiteTmemFull);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after_sync();
+      const int m0 = mb * (2 * kBM) + static_cast<int>(rank) * kBM + q * 32;
+      const int n0 = nb * p.bn;
+      const bool rows_live = m0 < p.M;
+      const int nchunks = (min(p.bn, p.N - n0) + kEpiCols - 1) / kEpiCols;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(acc * p.bn);
+      const uint32_t leader_tempty = mapa_shared(tempty_bar(acc), 0);
+      for (int c = 0; c < nchunks && rows_live; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(t_row + c * kEpiCols, r);
+        tmem_ld_wait();
+        if (c == nchunks - 1) {
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(leader_tempty);
+        }
+        const uint32_t buf = my_bufs + (chunk_seq % kEpiBufs) * kEpiChunkBytes;
+        if (chunk_seq >= static_cast<uint32_t>(kEpiBufs)) {
+          if (lane == 0) bulk_wait_group_read<kEpiBufs - 1>();
+          __syncwarp();
+        }
+        const uint32_t row_addr = buf + lane * 64u;
+        const uint32_t sw = (lane >> 1) & 3u;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          st_shared_v4(row_addr + ((j ^ sw) << 4), pack_half2(r[8 * j + 0], r[8 * j + 1]),
+                       pack_half2(r[8 * j + 2], r[8 * j + 3]),
+                       pack_half2(r[8 * j + 4], r[8 * j + 5]),
+                       pack_half2(r[8 * j + 6], r[8 * j + 7]));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tmD, buf, n0 + c * kEpiCols, m0);
+          bulk_commit_group();
+        }
+        ++chunk_seq;
+      }
+      if (!rows_live) {
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(leader_tempty);
+      }
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if (lane == 0) bulk_wait_group_all();
+    __syncwarp();
+  }
+
+  __syncwarp();
+  tc_fence_before_sync();
+  cluster_sync();  // no remote arrive or multicast commit targets a CTA that has left
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc_pair(tmem_base, p.tmem_cols);
+  }
+}
+
+}  // namespace gb300

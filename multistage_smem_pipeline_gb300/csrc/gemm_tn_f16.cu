@@ -9,7 +9,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "gemm_kernel.cuh"
+#include "gemm_pair_kernel.cuh"
 #include "gemm_tn_f16.h"
 
 namespace gb300 {
@@ -28,7 +28,9 @@ struct DeviceState {
   bool init = false;
   int status = GEMM_OK;
   int sm_count = 0;
-  int smem_attr = 0;  // dynamic smem size last granted to the kernel
+  int smem_attr = 0;       // dynamic smem granted to the single-CTA kernel
+  int pair_smem_attr = 0;  // ... and to the pair kernel
+  int max_pairs = 0;       // co-resident 2-CTA clusters at full shared memory
 };
 
 std::mutex g_mu;
@@ -74,14 +76,6 @@ int current_device(int* dev_out, DeviceState** st_out) {
   return st.status;
 }
 
-int sm_count_or_default() {
-  int dev = 0;
-  DeviceState* st = nullptr;
-  if (current_device(&dev, &st) == GEMM_OK) return st->sm_count;
-  cudaGetLastError();
-  return 148;
-}
-
 uint32_t pow2_at_least(uint32_t x) {
   uint32_t p = 32;
   while (p < x) p <<= 1;
@@ -95,8 +89,7 @@ uint32_t make_idesc(int m, int n) {
   return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 
-int stages_that_fit(int bn) {
-  const uint32_t stage_bytes = kABytes + static_cast<uint32_t>(bn) * 128u;
+int stages_that_fit(uint32_t stage_bytes) {
   const uint32_t fixed = kEpiWarps * kEpiBufs * kEpiChunkBytes + 16 + 1024;
   int s = 2;
   while (s + 1 <= kMaxStages) {
@@ -107,61 +100,93 @@ int stages_that_fit(int bn) {
   return s;
 }
 
-// Relative time of one k-block on one SM for a 128 x bn tile: the tensor
-// pipe needs 2*bn cycles (128 x bn x 64 MACs at 8192 flop/clk), the operand
-// reads from shared memory need (16 KiB + bn*128 B) / 128 B/clk.
-double kblock_cost(int bn) { return std::max(2.0 * bn, 128.0 + bn); }
+// Relative time of one k-block on one SM: the tensor pipe needs 2*n cycles
+// for its 128 x n x 64 block (8192 flop/clk/SM), and the stage must be
+// refilled at the rate the ring sustains with every SM loading -- about
+// 60 B/clk per SM measured on GB300 with a 4-6 deep ring.
+double kblock_cost(int n_per_sm, uint32_t stage_bytes) {
+  return std::max(2.0 * n_per_sm, static_cast<double>(stage_bytes) / 60.0);
+}
+
+uint32_t stage_bytes_for(int path, int bn) {
+  const int b_rows = (path == GEMM_PATH_PAIR) ? bn / 2 : bn;
+  return kABytes + static_cast<uint32_t>(b_rows) * 128u;
+}
 
 struct Plan {
   gemm_config_t cfg;
   GemmParams p;
 };
 
-int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sms, Plan* out) {
+int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sms, int max_pairs,
+              Plan* out) {
   gemm_options_t o;
   std::memset(&o, 0, sizeof(o));
   if (opt) o = *opt;
-  if (o.path < 0 || o.path > 2 || o.bn < 0 || o.bn > 256 || (o.bn % 32) != 0 || o.kstage < 0 ||
+  if (o.path < 0 || o.path > 3 || o.bn < 0 || o.bn > 256 || (o.bn % 32) != 0 || o.kstage < 0 ||
       o.kstage == 1 || o.kstage > kMaxStages || o.max_ctas < 0 || o.group_m < 0 || o.inject < 0 ||
       o.inject > 1)
     return GEMM_ERR_INVALID_VALUE;
-  int path = o.path;
-  if (path == GEMM_PATH_AUTO) path = (M <= kBM) ? GEMM_PATH_SKINNY : GEMM_PATH_SQUARE;
-  if (path == GEMM_PATH_SKINNY && M > kBM) return GEMM_ERR_INVALID_VALUE;
-
-  const int64_t num_m = (M + kBM - 1) / kBM;
+  if (o.path == GEMM_PATH_SKINNY && M > kBM) return GEMM_ERR_INVALID_VALUE;
+  if (max_pairs < 1) max_pairs = std::max(1, sms / 2);
   const int64_t num_k = (K + kBK - 1) / kBK;
-  int bn = o.bn;
-  if (bn == 0) {
-    // Fewest waves x per-k-block cost; ties go to the wider tile (less L2 traffic).
-    double best = 0;
+
+  // Candidates: (path, bn).  Cost = waves x k-blocks x per-k-block cost; ties
+  // go to the pair path, then to the wider tile (less L2 traffic).
+  int path = 0, bn = 0;
+  double best = 0;
+  for (int cp = 3; cp >= 1; --cp) {
+    if (cp == GEMM_PATH_SKINNY) continue;
+    int kind = cp;
+    if (o.path != GEMM_PATH_AUTO) {
+      const int want = (o.path == GEMM_PATH_SKINNY) ? GEMM_PATH_SQUARE : o.path;
+      if (kind != want) continue;
+    } else if (kind == GEMM_PATH_PAIR && M <= kBM) {
+      continue;  // a pair tile would be at least half empty
+    }
     for (int cand = 256; cand >= 32; cand -= 32) {
-      const int64_t tiles = num_m * ((N + cand - 1) / cand);
-      const int64_t waves = (tiles + sms - 1) / sms;
-      const double cost = static_cast<double>(waves) * kblock_cost(cand);
+      if (o.bn && cand != o.bn) continue;
+      const int bm = (kind == GEMM_PATH_PAIR) ? 2 * kBM : kBM;
+      const int64_t tiles = ((M + bm - 1) / bm) * ((N + cand - 1) / cand);
+      const int64_t slots = (kind == GEMM_PATH_PAIR) ? max_pairs : sms;
+      const int64_t waves = (tiles + slots - 1) / slots;
+      const double cost = static_cast<double>(waves) * static_cast<double>(num_k) *
+                          kblock_cost(cand, stage_bytes_for(kind, cand));
       if (bn == 0 || cost < best * (1.0 - 1e-9)) {
         best = cost;
         bn = cand;
+        path = kind;
       }
     }
   }
+  if (bn == 0) return GEMM_ERR_INVALID_VALUE;
+  if (path == GEMM_PATH_SQUARE && M <= kBM && o.path != GEMM_PATH_SQUARE) path = GEMM_PATH_SKINNY;
+
+  const int bm = (path == GEMM_PATH_PAIR) ? 2 * kBM : kBM;
+  const int64_t num_m = (M + bm - 1) / bm;
   const int64_t num_n = (N + bn - 1) / bn;
   const int64_t tiles = num_m * num_n;
   if (tiles > INT_MAX || num_k > INT_MAX) return GEMM_ERR_INVALID_VALUE;
-  const int fit = stages_that_fit(bn);
+  const uint32_t stage_bytes = stage_bytes_for(path, bn);
+  const int fit = stages_that_fit(stage_bytes);
   const int stages = o.kstage ? o.kstage : fit;
   if (stages > fit) return GEMM_ERR_INVALID_VALUE;
-  int ctas = static_cast<int>(std::min<int64_t>(tiles, sms));
-  if (o.max_ctas) ctas = std::min(ctas, o.max_ctas);
-  const int group_m = o.group_m ? o.group_m : 16;
-
-  const uint32_t stage_bytes = kABytes + static_cast<uint32_t>(bn) * 128u;
+  int ctas;
+  if (path == GEMM_PATH_PAIR) {
+    int64_t pairs = std::min<int64_t>(tiles, max_pairs);
+    if (o.max_ctas) pairs = std::min<int64_t>(pairs, std::max(1, o.max_ctas / 2));
+    ctas = static_cast<int>(2 * pairs);
+  } else {
+    ctas = static_cast<int>(std::min<int64_t>(tiles, sms));
+    if (o.max_ctas) ctas = std::min(ctas, o.max_ctas);
+  }
+  const int group_m = o.group_m ? o.group_m : (path == GEMM_PATH_PAIR ? 8 : 16);
   const SmemLayout L = SmemLayout::make(stages, stage_bytes);
 
   Plan pl;
   std::memset(&pl, 0, sizeof(pl));
   pl.cfg.path = path;
-  pl.cfg.bm = kBM;
+  pl.cfg.bm = bm;
   pl.cfg.bn = bn;
   pl.cfg.bk = kBK;
   pl.cfg.kstage = stages;
@@ -182,7 +207,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   p.num_k_blocks = static_cast<int32_t>(num_k);
   p.num_tiles = static_cast<int32_t>(tiles);
   p.group_m = group_m;
-  p.idesc = make_idesc(kBM, bn);
+  p.idesc = make_idesc(bm, bn);
   p.tmem_cols = pow2_at_least(2u * bn);
   p.stage_bytes = stage_bytes;
   p.l2_hints = (path == GEMM_PATH_SKINNY) ? 3u : 0u;
@@ -203,6 +228,42 @@ int encode_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_INVALID_VALUE;
+}
+
+// Grant both kernels the full dynamic shared memory and find how many
+// 2-CTA clusters can be resident at once (the pair path's persistent grid).
+int prepare_device(DeviceState* st) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (st->smem_attr == kMaxDynSmem && st->pair_smem_attr == kMaxDynSmem && st->max_pairs > 0)
+    return GEMM_OK;
+  if (cudaFuncSetAttribute(gemm_tn_f16_persistent, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kMaxDynSmem) != cudaSuccess ||
+      cudaFuncSetAttribute(gemm_tn_f16_pair, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kMaxDynSmem) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  st->smem_attr = st->pair_smem_attr = kMaxDynSmem;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2 * (st->sm_count / 2), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kMaxDynSmem;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, gemm_tn_f16_pair, &cfg) != cudaSuccess ||
+      clusters < 1) {
+    cudaGetLastError();
+    clusters = st->sm_count / 2;
+  }
+  st->max_pairs = std::min(clusters, st->sm_count / 2);
+  return GEMM_OK;
 }
 
 bool overlaps(const void* a, uint64_t abytes, const void* b, uint64_t bbytes) {
@@ -232,7 +293,7 @@ int run(void* D, const void* A, const void* B, int64_t M, int64_t N, int64_t K,
   if (opt) {  // validate options even when there is nothing to compute
     Plan tmp;
     rc = make_plan(std::max<int64_t>(M, 1), std::max<int64_t>(N, 8), std::max<int64_t>(K, 8), opt,
-                   148, &tmp);
+                   148, 74, &tmp);
     if (rc != GEMM_OK) return rc;
   }
   if (M == 0 || N == 0) return GEMM_OK;
@@ -247,30 +308,42 @@ int run(void* D, const void* A, const void* B, int64_t M, int64_t N, int64_t K,
     }
     return GEMM_OK;
   }
+  if ((rc = prepare_device(st)) != GEMM_OK) return rc;
   Plan pl;
-  rc = make_plan(M, N, K, opt, st->sm_count, &pl);
+  rc = make_plan(M, N, K, opt, st->sm_count, st->max_pairs, &pl);
   if (rc != GEMM_OK) return rc;
   if ((rc = get_encoder()) != GEMM_OK) return rc;
 
+  const bool pair = pl.cfg.path == GEMM_PATH_PAIR;
+  const uint32_t b_box_rows = pair ? pl.cfg.bn / 2 : pl.cfg.bn;
   CUtensorMap tmA, tmB, tmD;
   if (encode_2d(&tmA, A, K, M, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B) != GEMM_OK ||
-      encode_2d(&tmB, B, K, N, kBK, pl.cfg.bn, CU_TENSOR_MAP_SWIZZLE_128B) != GEMM_OK ||
+      encode_2d(&tmB, B, K, N, kBK, b_box_rows, CU_TENSOR_MAP_SWIZZLE_128B) != GEMM_OK ||
       encode_2d(&tmD, D, N, M, kEpiCols, 32, CU_TENSOR_MAP_SWIZZLE_64B) != GEMM_OK)
     return GEMM_ERR_INVALID_VALUE;
 
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (st->smem_attr < pl.cfg.smem_bytes) {
-      if (cudaFuncSetAttribute(gemm_tn_f16_persistent, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kMaxDynSmem) != cudaSuccess) {
-        cudaGetLastError();
-        return GEMM_ERR_CUDA;
-      }
-      st->smem_attr = kMaxDynSmem;
+  if (!pair) {
+    gemm_tn_f16_persistent<<<pl.cfg.ctas, kThreads, pl.cfg.smem_bytes, stream>>>(tmA, tmB, tmD,
+                                                                                 pl.p);
+  } else {
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(pl.cfg.ctas, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = pl.cfg.smem_bytes;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, gemm_tn_f16_pair, tmA, tmB, tmD, pl.p) != cudaSuccess) {
+      cudaGetLastError();
+      return GEMM_ERR_LAUNCH;
     }
   }
-  gemm_tn_f16_persistent<<<pl.cfg.ctas, kThreads, pl.cfg.smem_bytes, stream>>>(tmA, tmB, tmD,
-                                                                               pl.p);
   if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
   return GEMM_OK;
 }
@@ -294,8 +367,16 @@ extern "C" int gemm_query_config(int64_t M, int64_t N, int64_t K, const gemm_opt
                                  gemm_config_t* out) {
   if (!out || M <= 0 || N <= 0 || K <= 0 || M > INT_MAX || N > INT_MAX || K > INT_MAX)
     return GEMM_ERR_INVALID_VALUE;
+  int sms = 148, pairs = 74, dev = 0;
+  DeviceState* st = nullptr;
+  if (current_device(&dev, &st) == GEMM_OK && prepare_device(st) == GEMM_OK) {
+    sms = st->sm_count;
+    pairs = st->max_pairs;
+  } else {
+    cudaGetLastError();
+  }
   Plan pl;
-  const int rc = make_plan(M, N, K, opt, sm_count_or_default(), &pl);
+  const int rc = make_plan(M, N, K, opt, sms, pairs, &pl);
   if (rc == GEMM_OK) *out = pl.cfg;
   return rc;
 }

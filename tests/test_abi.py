@@ -96,7 +96,7 @@ def test_empty_output_is_a_noop_without_device(binding):
 
 
 def test_rejects_bad_options(binding):
-    for kw in [dict(bn=48), dict(bn=512), dict(kstage=1), dict(kstage=17), dict(path=3),
+    for kw in [dict(bn=48), dict(bn=512), dict(kstage=1), dict(kstage=17), dict(path=4),
                dict(inject=2), dict(max_ctas=-1), dict(path=binding.PATH_SKINNY)]:
         o = binding._options(**kw)
         M = 256 if kw.get("path") == binding.PATH_SKINNY else 64
@@ -111,21 +111,27 @@ def test_valid_call_without_a_device_reports_cuda_error(binding):
 
 def test_query_config_plans(binding):
     c = binding.query_config(8192, 8192, 8192)
-    assert c["path"] == binding.PATH_SQUARE and c["bm"] == 128 and c["bk"] == 64
+    assert c["path"] == binding.PATH_PAIR and c["bm"] == 256 and c["bk"] == 64
+    assert c["ctas"] % 2 == 0
     assert c["bn"] % 32 == 0 and 32 <= c["bn"] <= 256
     assert c["kstage"] >= 2 and c["smem_bytes"] <= 232448
     assert c["tmem_cols"] >= 2 * c["bn"] and c["tmem_cols"] <= 512
     assert c["tmem_cols"] & (c["tmem_cols"] - 1) == 0
     s = binding.query_config(128, 14336, 4096)
     assert s["path"] == binding.PATH_SKINNY and s["tiles"] <= s["ctas"] * 2
-    # every explicit (bn, kstage) that is accepted fits the shared-memory budget
-    for bn in range(32, 257, 32):
-        deepest = binding.query_config(1024, 1024, 1024, bn=bn)["kstage"]
-        for ks in range(2, deepest + 1):
-            cc = binding.query_config(1024, 1024, 1024, bn=bn, kstage=ks)
-            assert cc["smem_bytes"] <= 232448 and cc["kstage"] == ks
-        with pytest.raises(binding.GemmError):
-            binding.query_config(1024, 1024, 1024, bn=bn, kstage=deepest + 1)
+    # every explicit (path, bn, kstage) that is accepted fits the shared-memory budget
+    for path in (binding.PATH_SQUARE, binding.PATH_PAIR):
+        for bn in range(32, 257, 32):
+            deepest = binding.query_config(1024, 1024, 1024, path=path, bn=bn)["kstage"]
+            for ks in range(2, deepest + 1):
+                cc = binding.query_config(1024, 1024, 1024, path=path, bn=bn, kstage=ks)
+                assert cc["smem_bytes"] <= 232448 and cc["kstage"] == ks and cc["path"] == path
+                assert cc["bm"] == (256 if path == binding.PATH_PAIR else 128)
+            with pytest.raises(binding.GemmError):
+                binding.query_config(1024, 1024, 1024, path=path, bn=bn, kstage=deepest + 1)
+    # a pair stage holds half of B, so the pair ring is deeper at the same width
+    assert binding.query_config(4096, 4096, 4096, path=binding.PATH_PAIR, bn=256)["kstage"] > \
+        binding.query_config(4096, 4096, 4096, path=binding.PATH_SQUARE, bn=256)["kstage"]
 
 
 def test_status_strings(binding):

@@ -20,20 +20,21 @@ def lib(gpu):
     return binding
 
 
-def test_stalled_stage_times_out_and_context_survives(lib, gpu):
+@pytest.mark.parametrize("path", [1, 3])
+def test_stalled_stage_times_out_and_context_survives(lib, gpu, path):
     a_bits = synthetic.uniform_pm1(1, (256, 512))
     b_bits = synthetic.uniform_pm1(2, (512, 512))
     a = torch.from_numpy(a_bits.view(np.float16)).to(gpu)
     b = torch.from_numpy(b_bits.view(np.float16)).to(gpu)
     assert lib.get_device_error()[0] == lib.GEMM_OK           # clean slate
-    lib.gemm_tn_f16_ex(a, b, inject=1, timeout_ns=50_000_000, max_ctas=2)
+    lib.gemm_tn_f16_ex(a, b, inject=1, timeout_ns=50_000_000, max_ctas=2, path=path)
     status, raw = lib.get_device_error()
     assert status == lib.GEMM_ERR_TIMEOUT
     assert (raw >> 8) in (1, 2, 3, 4)                          # the site that gave up
     assert lib.get_device_error()[0] == lib.GEMM_OK            # reading clears it
     # the same SMs run a normal GEMM correctly afterwards (TMEM was freed)
     for _ in range(2):
-        d = lib.gemm_tn_f16(a, b)
+        d = lib.gemm_tn_f16_ex(a, b, path=path)
         torch.cuda.synchronize()
         st = compare(d.cpu().numpy().view(np.uint16), oracle.gemm_tn(a_bits, b_bits), 512,
                      a_bits, b_bits)

@@ -64,37 +64,54 @@ def test_shapes_with_tails(lib, gpu, M, N, K):
     _check(_run(lib, a, b, gpu), a, b)
 
 
+SQUARE, PAIR = 1, 3
+
+
+@pytest.mark.parametrize("path", [SQUARE, PAIR])
 @pytest.mark.parametrize("bn", list(range(32, 257, 32)))
-def test_every_tile_width(lib, gpu, bn):
-    M, N, K = 272, 8 * 83, 328          # 3 m-blocks, ragged n, 6 k-blocks (tail 8)
+def test_every_tile_width(lib, gpu, bn, path):
+    M, N, K = 272, 8 * 83, 328          # ragged m-blocks, ragged n, 6 k-blocks (tail 8)
     a = synthetic.uniform_pm1(bn, (M, K))
     b = synthetic.uniform_pm1(bn + 1, (N, K))
-    _check(_run(lib, a, b, gpu, bn=bn), a, b)
+    _check(_run(lib, a, b, gpu, bn=bn, path=path), a, b)
 
 
-@pytest.mark.parametrize("bn", [256, 128, 64])
-def test_every_ring_depth_and_wrap(lib, gpu, bn):
+@pytest.mark.parametrize("path,bn", [(SQUARE, 256), (SQUARE, 128), (SQUARE, 64),
+                                     (PAIR, 256), (PAIR, 128), (PAIR, 64)])
+def test_every_ring_depth_and_wrap(lib, gpu, path, bn):
     # K = BK * (kstage +- 1) around every depth: the ring wraps mid-tile and
-    # the phase bits flip at different k-blocks; one CTA walks all tiles so
-    # both TMEM accumulators are reused many times.
-    deepest = lib.query_config(256, 512, 4096, bn=bn)["kstage"]
-    a_full = synthetic.uniform_pm1(5, (256, 64 * (deepest + 2)))
+    # the phase bits flip at different k-blocks; one CTA (pair) walks all
+    # tiles so both TMEM accumulators are reused many times.
+    deepest = lib.query_config(256, 512, 4096, bn=bn, path=path)["kstage"]
+    a_full = synthetic.uniform_pm1(5, (512, 64 * (deepest + 2)))
     b_full = synthetic.uniform_pm1(6, (512, 64 * (deepest + 2)))
     for ks in range(2, deepest + 1):
         for kb in (ks - 1, ks, ks + 1):
             K = 64 * kb
             a = np.ascontiguousarray(a_full[:, :K])
             b = np.ascontiguousarray(b_full[:, :K])
-            got = _run(lib, a, b, gpu, bn=bn, kstage=ks, max_ctas=1)
+            got = _run(lib, a, b, gpu, bn=bn, kstage=ks, max_ctas=2 if path == PAIR else 1,
+                       path=path)
             _check(got, a, b)
 
 
-@pytest.mark.parametrize("ctas,group_m", [(1, 1), (3, 2), (5, 16), (0, 3)])
-def test_persistent_schedules(lib, gpu, ctas, group_m):
+@pytest.mark.parametrize("path", [SQUARE, PAIR])
+@pytest.mark.parametrize("ctas,group_m", [(2, 1), (6, 2), (10, 16), (0, 3)])
+def test_persistent_schedules(lib, gpu, ctas, group_m, path):
     M, N, K = 128 * 5 + 17, 256 * 3 + 40, 192
     a = synthetic.uniform_pm1(ctas + 40, (M, K))
     b = synthetic.uniform_pm1(group_m + 50, (N, K))
-    _check(_run(lib, a, b, gpu, max_ctas=ctas, group_m=group_m, bn=128), a, b)
+    _check(_run(lib, a, b, gpu, max_ctas=ctas, group_m=group_m, bn=128, path=path), a, b)
+
+
+@pytest.mark.parametrize("M", [129, 200, 256, 300, 384, 385, 640])
+def test_pair_row_tails(lib, gpu, M):
+    # M not a multiple of 256: the odd CTA of the last pair has few or no
+    # valid rows but still feeds its zero-filled half of the MMA
+    N, K = 264, 136
+    a = synthetic.uniform_pm1(M, (M, K))
+    b = synthetic.uniform_pm1(M + 3, (N, K))
+    _check(_run(lib, a, b, gpu, path=PAIR), a, b)
 
 
 def test_skinny_path_small(lib, gpu):

@@ -240,6 +240,9 @@ def run_gpu(args, tag):
     d = torch.empty((M, N), dtype=torch.float16, device=dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    clean = torch.zeros(2 * l2 // 4, dtype=torch.int32, device=dev) if args.flush == "write+read" \
+        else None
+    sleep_cycles = int(args.launch_slack_us * 2.0e3)   # ~2 GHz SM clock
     stream = torch.cuda.current_stream(dev)
     opts = {"path": ["auto", "square", "skinny", "pair"].index(args.path), "bn": args.bn,
             "kstage": args.kstage}
@@ -268,6 +271,12 @@ def run_gpu(args, tag):
     wall0 = time.perf_counter()
     for i in range(args.steps):
         flush.zero_()                           # evict A, B, D from L2 (not timed)
+        if clean is not None:
+            clean.sum()                         # replace the dirty flush lines with clean ones
+        if sleep_cycles:
+            # keep the GPU busy while the host enqueues the timed launch, so the
+            # start event does not wait on host-side launch overhead
+            torch.cuda._sleep(sleep_cycles)
         starts[i].record(stream)
         gemm(a, b)
         ends[i].record(stream)
@@ -278,6 +287,21 @@ def run_gpu(args, tag):
     clk = clocks.stop()
     launches_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms = statistics.mean(launches_ms)
+    # the same launches after a write-only flush (dirty flush lines left in L2)
+    alt_ms = None
+    if clean is not None and args.alt_steps > 0:
+        n_alt = min(args.steps, args.alt_steps)
+        s_alt = [torch.cuda.Event(enable_timing=True) for _ in range(n_alt)]
+        e_alt = [torch.cuda.Event(enable_timing=True) for _ in range(n_alt)]
+        for i in range(n_alt):
+            flush.zero_()
+            if sleep_cycles:
+                torch.cuda._sleep(sleep_cycles)
+            s_alt[i].record(stream)
+            gemm(a, b)
+            e_alt[i].record(stream)
+        torch.cuda.synchronize(dev)
+        alt_ms = statistics.mean([x.elapsed_time(y) for x, y in zip(s_alt, e_alt)])
     if world > 1:
         t = torch.tensor([ms], dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -334,8 +358,10 @@ def run_gpu(args, tag):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
             "data": "synthetic (seeded splitmix64, fp16-rounded)",
             "config": workload_config(tag, spec, {
-                "l2": "flushed before every timed launch (2 x L2 bytes written, outside the "
-                      "launch's event pair)",
+                "l2": ("flushed before every timed launch: 2 x L2 bytes written" +
+                       (", then 2 x L2 bytes of a clean buffer read" if clean is not None else "") +
+                       ", outside the launch's event pair"),
+                "launch_slack_us": args.launch_slack_us,
                 "path": ["auto", "square", "skinny", "pair"][cfg["path"]], "bm": cfg["bm"],
                 "bn": cfg["bn"], "bk": cfg["bk"], "kstage": cfg["kstage"], "ctas": cfg["ctas"],
                 "tiles": cfg["tiles"], "forced": forced}),
@@ -343,10 +369,11 @@ def run_gpu(args, tag):
                           "p10": float(np.percentile(launches_ms, 10)),
                           "p90": float(np.percentile(launches_ms, 90))},
             "roofline": roof,
+            "launch_ms_write_only_flush": alt_ms,
             "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                     "h2d_bytes_per_step": 2 * (M * K + N * K), "d2h_bytes_per_step": 2 * M * N,
                     "ms_per_step": e2e_ms, "steps": e2e_steps},
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps + (min(args.steps, args.alt_steps) if alt_ms else 0),
             "clocks": clk,
             "wall_s_timed_region": wall}
     if world == 1 and not args.no_cpu:
@@ -371,6 +398,13 @@ def main():
     ap.add_argument("--reference-budget", type=float, default=90.0,
                     help="target wall seconds for the whole --impl reference run")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--flush", choices=["write", "write+read"], default="write+read",
+                    help="L2 flush before each timed launch: write 2 x L2 bytes, optionally "
+                         "followed by reading a clean buffer of that size")
+    ap.add_argument("--alt-steps", type=int, default=100,
+                    help="extra launches timed after a write-only flush (reported, not the value)")
+    ap.add_argument("--launch-slack-us", type=float, default=100.0,
+                    help="device-side sleep before each start event (outside the timed pair)")
     ap.add_argument("--path", choices=["auto", "square", "skinny", "pair"], default="auto",
                     help="diagnostics: force a kernel path (default: the library's choice)")
     ap.add_argument("--bn", type=int, default=0, help="diagnostics: force the tile width")

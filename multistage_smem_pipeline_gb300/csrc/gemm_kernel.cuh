@@ -121,7 +121,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         int mb, nb;
         tile_coords(t, p, mb, nb);
         bool ok = true;
-        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        const int k0 = first_k_block(t, p);
+        for (int i = 0; i < p.num_k_blocks; ++i) {
+          const int kb = (k0 + i < p.num_k_blocks) ? k0 + i : k0 + i - p.num_k_blocks;
           if (!wait_or_abort(empty_bar(stage), phase ^ 1u, p.timeout_ns, abort_flag, kSiteEmpty)) {
             ok = false;
             break;
@@ -167,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * p.bn);
         bool ok = true;
-        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        for (int i = 0; i < p.num_k_blocks; ++i) {
           if (!wait_or_abort(full_bar(stage), phase, p.timeout_ns, abort_flag, kSiteFull)) {
             ok = false;
             break;
@@ -180,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < kBK / kUmmaK; ++k) {
             // +32 bytes along K inside the 128-byte swizzle row = +2 in the
             // descriptor's address field (16-byte units)
-            umma_f16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, p.idesc, (kb | k) != 0);
+            umma_f16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, p.idesc, (i | k) != 0);
           }
           umma_commit(empty_bar(stage));  // frees the stage once these MMAs have read it
           if (++stage == S) {

@@ -96,6 +96,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer (both CTAs)
     if (lane == 0) {
       const uint64_t pol_a = l2_policy_evict_last();
+      const uint64_t pol_b = l2_policy_evict_first();
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0;
@@ -105,7 +106,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int a_row = mb * (2 * kBM) + static_cast<int>(rank) * kBM;
         const int b_row = nb * p.bn + static_cast<int>(rank) * half_bn;
         bool ok = true;
-        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        const int k0 = first_k_block(t, p);
+        for (int i = 0; i < p.num_k_blocks; ++i) {
+          const int kb = (k0 + i < p.num_k_blocks) ? k0 + i : k0 + i - p.num_k_blocks;
           if (!wait_or_abort(empty_bar(stage), phase ^ 1u, p.timeout_ns, abort_flag, kSiteEmpty)) {
             ok = false;
             break;
@@ -119,7 +122,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_load_2d_pair_hint(a_dst, &tmA, leader_full, kb * kBK, a_row, pol_a);
             else
               tma_load_2d_pair(a_dst, &tmA, leader_full, kb * kBK, a_row);
-            tma_load_2d_pair(b_dst, &tmB, leader_full, kb * kBK, b_row);
+            if (p.l2_hints & 1u)
+              tma_load_2d_pair_hint(b_dst, &tmB, leader_full, kb * kBK, b_row, pol_b);
+            else
+              tma_load_2d_pair(b_dst, &tmB, leader_full, kb * kBK, b_row);
           }
           ++issued;
           if (++stage == S) {
@@ -149,7 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * p.bn);
         bool ok = true;
-        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        for (int i = 0; i < p.num_k_blocks; ++i) {
           if (!wait_or_abort(full_bar(stage), phase, p.timeout_ns, abort_flag, kSiteFull)) {
             ok = false;
             break;
@@ -160,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t b_desc = sw128_kmajor_desc(a_src + kABytes);
 #pragma unroll
           for (int k = 0; k < kBK / kUmmaK; ++k)
-            umma_f16_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, p.idesc, (kb | k) != 0);
+            umma_f16_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, p.idesc, (i | k) != 0);
           umma_commit_pair_mc(empty_bar(stage), 0x3);
           if (++stage == S) {
             stage = 0;

@@ -210,7 +210,10 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   p.idesc = make_idesc(bm, bn);
   p.tmem_cols = pow2_at_least(2u * bn);
   p.stage_bytes = stage_bytes;
-  p.l2_hints = (path == GEMM_PATH_SKINNY) ? 3u : 0u;
+  // One m-block: every tile reads the same rows of A (keep them in L2, stream
+  // B through it once) and the k loops are rotated across tiles.
+  p.l2_hints = (num_m == 1) ? 3u : 0u;
+  p.k_rotate = (num_m == 1 && num_n > 1) ? 1 : 0;
   p.timeout_ns = o.timeout_ns ? o.timeout_ns : kDefaultTimeoutNs;
   p.inject = o.inject;
   *out = pl;

@@ -36,7 +36,18 @@ struct GemmParams {
   uint32_t l2_hints;     // bit 0: stream B with evict-first; bit 1: keep A with evict-last
   uint64_t timeout_ns;
   int32_t inject;
+  int32_t k_rotate;      // 1: each tile starts its k loop at a tile-dependent k-block
 };
+
+// First k-block of tile t.  With rotation the tiles in flight start at
+// evenly spread k offsets, so when every tile reads the same rows of A (one
+// m-block) they do not all hit the same L2 lines at the same moment.  Only
+// the order of the fp32 accumulation changes.
+__device__ __forceinline__ int first_k_block(int t, const GemmParams& p) {
+  if (!p.k_rotate) return 0;
+  return static_cast<int>((static_cast<int64_t>(t) * p.num_k_blocks) / p.num_tiles) %
+         p.num_k_blocks;
+}
 
 // Shared-memory carve-up, offsets from the 1024-aligned base.
 struct SmemLayout {

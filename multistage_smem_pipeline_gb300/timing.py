@@ -9,8 +9,11 @@ import numpy as np
 import torch
 
 
-def time_launches(launch, steps: int, warmup: int, device=None, flush: bool = True) -> dict:
-    """Call `launch()` warmup + steps times; return per-launch ms statistics."""
+def time_launches(launch, steps: int, warmup: int, device=None, flush: bool = True,
+                  slack_cycles: int = 200_000) -> dict:
+    """Call `launch()` warmup + steps times; return per-launch ms statistics.
+    A device-side sleep of `slack_cycles` precedes each start event so that the
+    host has enqueued the launch before the timed interval opens."""
     dev = torch.device(device or "cuda")
     stream = torch.cuda.current_stream(dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -23,6 +26,8 @@ def time_launches(launch, steps: int, warmup: int, device=None, flush: bool = Tr
     for i in range(steps):
         if buf is not None:
             buf.zero_()
+        if slack_cycles:
+            torch.cuda._sleep(slack_cycles)
         starts[i].record(stream)
         launch()
         ends[i].record(stream)

@@ -114,6 +114,28 @@ def test_pair_row_tails(lib, gpu, M):
     _check(_run(lib, a, b, gpu, path=PAIR), a, b)
 
 
+@pytest.mark.parametrize("path", [SQUARE, PAIR])
+def test_one_m_block_rotated_k_is_bit_exact_on_ternary(lib, gpu, path):
+    # M <= 128 rotates each tile's k loop; integer partial sums are exact in
+    # any order, so the result must still match bit for bit
+    a = synthetic.ternary(21, (128, 1024))
+    b = synthetic.ternary(22, (1000, 1024))
+    got = _run(lib, a, b, gpu, path=path)
+    ai = a.view(np.float16).astype(np.int64)
+    bi = b.view(np.float16).astype(np.int64)
+    assert np.array_equal(got, (ai @ bi.T).astype(np.float16).view(np.uint16))
+    assert np.array_equal(got, oracle.gemm_tn(a, b))
+
+
+@pytest.mark.parametrize("bn", [64, 192, 256])
+def test_pair_path_with_one_row_block(lib, gpu, bn):
+    # M <= 128 on the pair path: the odd CTA's A rows are all out of range
+    for M in (1, 77, 128):
+        a = synthetic.gaussian(M + 5, (M, 640))
+        b = synthetic.gaussian(M + 6, (1400, 640), 0.02)
+        _check(_run(lib, a, b, gpu, path=PAIR, bn=bn), a, b)
+
+
 def test_skinny_path_small(lib, gpu):
     for M in (1, 16, 100, 128):
         a = synthetic.gaussian(M, (M, 512))

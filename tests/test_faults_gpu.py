@@ -9,7 +9,7 @@ import torch
 
 import oracle
 from multistage_smem_pipeline_gb300 import synthetic
-from tolerance import compare
+from tolerance import compare, probes_agree
 
 pytestmark = pytest.mark.gpu
 
@@ -47,3 +47,11 @@ def test_latency_probes_give_a_stage_count(lib, gpu):
     assert copy > 0 and compute > 0
     s = lib.minimum_stages(int(np.ceil(copy)), int(np.ceil(compute)))
     assert s >= 2
+    # a 128 x 256 x 64 k-block is 512 tensor-pipe cycles at the dense fp16 rate
+    assert 400 < compute < 1000
+
+
+def test_latency_probes_repeat_within_tolerance(lib, gpu):
+    first = lib.probe_latencies(bn=256, ctas=0, footprint_bytes=16 << 20, reps=64)
+    second = lib.probe_latencies(bn=256, ctas=0, footprint_bytes=16 << 20, reps=64)
+    assert probes_agree(first, second), (first, second)

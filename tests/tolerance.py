@@ -40,3 +40,17 @@ def compare(got_bits: np.ndarray, ref_bits: np.ndarray, K: int, a_bits: np.ndarr
             "max_ulps": int(ulps.max()) if ulps.size else 0,
             "exact_frac": float(np.mean(got_bits == ref_bits)) if got_bits.size else 1.0,
             "n": int(got_bits.size)}
+
+
+# Latency probes report cycle counts measured on a live GPU, so two
+# measurements of the same quantity agree only to within run-to-run noise.
+# Relative bounds used wherever two probe results are compared: the copy
+# latency (memory system, shared by all SMs) varies more than the MMA time.
+PROBE_REL_TOL = {"copy": 0.25, "compute": 0.05}
+
+
+def probes_agree(a: tuple, b: tuple) -> bool:
+    """(copy_cycles, compute_cycles) pairs within PROBE_REL_TOL of each other."""
+    (c1, m1), (c2, m2) = a, b
+    return (abs(c1 - c2) <= PROBE_REL_TOL["copy"] * max(c1, c2)
+            and abs(m1 - m2) <= PROBE_REL_TOL["compute"] * max(m1, m2))

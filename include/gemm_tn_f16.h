@@ -125,6 +125,27 @@ int64_t gemm_minimum_stages(int64_t copy_cycles, int64_t compute_cycles);
 int gemm_probe_latencies(int bn, int ctas, const void* scratch, int64_t footprint_bytes, int reps,
                          double* copy_cycles, double* compute_cycles, void* stream);
 
+/* gemm_probe_latencies_static: the same probes as gemm_probe_latencies for
+ * callers that cannot allocate device memory -- for example a serving process
+ * whose memory pool already holds nearly all of HBM, or a loop that must not
+ * call cudaMalloc/cudaFree because they can synchronise the device.  The
+ * pages have no counterpart to this entry point; it exists only for such
+ * callers.
+ *   - The copy probe loads from a fixed 16 MiB array in device memory owned by
+ *     the library (held on every GPU that loads it until the process exits);
+ *     footprint_bytes above 16 MiB returns GEMM_ERR_INVALID_VALUE, other
+ *     arguments are checked as in gemm_probe_latencies.  16 MiB fits in L2,
+ *     so copy_cycles is the L2-resident latency.
+ *   - Allocates nothing and calls no allocating routine.  The first call on a
+ *     device looks up the array's device address (set-up); make that first
+ *     call before any stream capture on the device.
+ *   - All calls share the array and the result counters (cleared at the start
+ *     of each call); calls that overlap on the GPU race and report wrong
+ *     numbers.
+ * Synchronous. */
+int gemm_probe_latencies_static(int bn, int ctas, int64_t footprint_bytes, int reps,
+                                double* copy_cycles, double* compute_cycles, void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* gemm_status_string(int status);
 

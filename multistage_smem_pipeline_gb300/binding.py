@@ -24,7 +24,8 @@ GEMM_ERR_CUDA = 6
 PATH_AUTO, PATH_SQUARE, PATH_SKINNY, PATH_PAIR = 0, 1, 2, 3
 
 EXPORTED = ("gemm_tn_f16", "gemm_tn_f16_ex", "gemm_query_config", "gemm_get_device_error",
-            "gemm_minimum_stages", "gemm_probe_latencies", "gemm_status_string")
+            "gemm_minimum_stages", "gemm_probe_latencies", "gemm_probe_latencies_static",
+            "gemm_status_string")
 
 
 class GemmOptions(ctypes.Structure):
@@ -68,6 +69,9 @@ def _load() -> ctypes.CDLL:
     lib.gemm_probe_latencies.argtypes = [i32, i32, vp, i64, i32, ctypes.POINTER(ctypes.c_double),
                                          ctypes.POINTER(ctypes.c_double), vp]
     lib.gemm_probe_latencies.restype = i32
+    lib.gemm_probe_latencies_static.argtypes = [i32, i32, i64, i32, ctypes.POINTER(ctypes.c_double),
+                                                ctypes.POINTER(ctypes.c_double), vp]
+    lib.gemm_probe_latencies_static.restype = i32
     lib.gemm_status_string.argtypes = [i32]
     lib.gemm_status_string.restype = ctypes.c_char_p
     return lib
@@ -184,4 +188,21 @@ def probe_latencies(bn: int = 256, ctas: int = 0, footprint_bytes: int = 1 << 30
                                       _stream_handle(None))
     if rc != GEMM_OK:
         raise GemmError(rc, "gemm_probe_latencies")
+    return c.value, m.value
+
+
+def probe_latencies_static(bn: int = 256, ctas: int = 0, footprint_bytes: int = 16 << 20,
+                           reps: int = 64, device=None) -> tuple[float, float]:
+    """(copy_cycles, compute_cycles) like probe_latencies, for callers that cannot
+    allocate device memory: the copy probe loads from the library's own 16 MiB
+    device array, so nothing is allocated here or in the library."""
+    dev = torch.device(device or "cuda")
+    c = ctypes.c_double(0)
+    m = ctypes.c_double(0)
+    with torch.cuda.device(dev):
+        rc = LIB.gemm_probe_latencies_static(int(bn), int(ctas), int(footprint_bytes), int(reps),
+                                             ctypes.byref(c), ctypes.byref(m),
+                                             _stream_handle(None))
+    if rc != GEMM_OK:
+        raise GemmError(rc, "gemm_probe_latencies_static")
     return c.value, m.value

@@ -8,6 +8,7 @@
 
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "pipeline.cuh"
 #include "gemm_tn_f16.h"
@@ -216,4 +217,69 @@ extern "C" int gemm_probe_latencies(int bn, int ctas, const void* scratch, int64
   probe_mma<<<1, 128, smem, s>>>(bn, cols, reps);
   if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
   return read_counters(s, compute_cycles);
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of gemm_probe_latencies.
+//
+// Some callers cannot call cudaMalloc: a serving process whose memory pool
+// has already reserved nearly all of HBM (a fresh allocation would fail or
+// make the pool give memory back), or a latency-sensitive loop that must not
+// allocate because cudaMalloc/cudaFree can synchronise the device.  For them
+// the copy probe's load footprint lives in a fixed array in device memory
+// that the library owns.  Every GPU that loads this library holds the array
+// (kStaticProbeScratchBytes) until the process exits.
+//
+// In host code the array's name is only a host-side stand-in for the device
+// symbol, never a device address: the device address is fetched once per
+// device with cudaGetSymbolAddress (with that device current) and cached.
+// That set-up happens in the entry point's first call on each device, so the
+// first call should come before any stream capture on that device.
+//
+// All calls share the array and the probes' result counters.  The array's
+// contents are never relied on (the probe only times loads of it), and the
+// counters are cleared at the start of every call; two calls that overlap
+// on the GPU (e.g. on different streams) race on the counters and report
+// wrong numbers.
+// ---------------------------------------------------------------------------
+namespace gb300 {
+namespace {
+
+constexpr int64_t kStaticProbeScratchBytes = 16ll << 20;  // 16 MiB per device
+static __device__ __align__(256) uint8_t g_probe_static_scratch[kStaticProbeScratchBytes];
+
+std::mutex g_static_mu;
+void* g_static_scratch_ptr[64];  // device address of the array, per device (nullptr = not set up)
+
+}  // namespace
+}  // namespace gb300
+
+extern "C" int gemm_probe_latencies_static(int bn, int ctas, int64_t footprint_bytes, int reps,
+                                           double* copy_cycles, double* compute_cycles,
+                                           void* stream) {
+  using namespace gb300;
+  if (footprint_bytes > kStaticProbeScratchBytes) return GEMM_ERR_INVALID_VALUE;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= 64) return GEMM_ERR_CUDA;
+  void* ptr = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_static_mu);
+    if (!g_static_scratch_ptr[dev]) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_probe_static_scratch) != cudaSuccess || !p) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+      }
+      g_static_scratch_ptr[dev] = p;
+    }
+    ptr = g_static_scratch_ptr[dev];
+  }
+  // Same probes, same checks (bn, ctas, reps, minimum footprint, device), on
+  // the library-owned array instead of a caller-allocated region.
+  return gemm_probe_latencies(bn, ctas, ptr, footprint_bytes, reps, copy_cycles, compute_cycles,
+                              stream);
 }

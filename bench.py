@@ -3,17 +3,20 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c1..c5] [--impl reference]
 
 A step is one gemm_tn_f16 call (the whole path: one persistent kernel) on
-seeded synthetic fp16 inputs already resident in HBM.  Before every timed
-launch the L2 is flushed by writing a buffer twice the L2 size; each launch
-is bracketed by CUDA events on its stream and ms_per_step is the mean launch
-time.  Default workload: 8192 x 8192 x 8192, U[-1, 1] operands.
+seeded synthetic fp16 inputs already resident in HBM.  The K timed steps run
+back to back between one pair of CUDA events on the launching stream, and
+cycle through R copies of A, B and D whose total exceeds 3 x L2, so each
+launch reads operands evicted from L2 by the launches in between (inputs
+larger than L2); ms_per_step = elapsed / K.  Default workload: 8192 x 8192 x
+8192, U[-1, 1] operands.
 
 Extra keys: roofline (the GEMM kernel against the measured dense bf16 peak,
 fp16 running at the same nominal rate, or against measured HBM bandwidth for
-the skinny case), cpu_baseline (the CPU oracle timed on a bounded row slice
-of the same workload on this host), e2e (host buffers: H2D of A and B, the
-GEMM, D2H of D, per step), clocks (nvidia-smi sampled during the timed
-region), gpu_launches.
+the skinny case), launch_ms_isolated (the same launch timed alone after an
+L2 flush, per-launch events: adds the isolated-launch latency), cpu_baseline
+(the CPU oracle timed on a bounded row slice of the same workload on this
+host), e2e (host buffers: H2D of A and B, the GEMM, D2H of D, per step),
+clocks (nvidia-smi sampled during the timed region), gpu_launches.
 
 --impl reference times the CPU oracle itself (the only other implementation
 of this computation here) on the same workload and metric.
@@ -237,71 +240,131 @@ def run_gpu(args, tag):
     b_host = torch.from_numpy(b_bits.view(np.float16)).pin_memory()
     a = a_host.to(dev)
     b = b_host.to(dev)
-    d = torch.empty((M, N), dtype=torch.float16, device=dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
-    clean = torch.zeros(2 * l2 // 4, dtype=torch.int32, device=dev) if args.flush == "write+read" \
-        else None
-    sleep_cycles = int(args.launch_slack_us * 2.0e3)   # ~2 GHz SM clock
     stream = torch.cuda.current_stream(dev)
     opts = {"path": ["auto", "square", "skinny", "pair"].index(args.path), "bn": args.bn,
-            "kstage": args.kstage}
+            "kstage": args.kstage, "katoms": args.katoms, "group_m": args.group_m}
     forced = any(opts.values())
     cfg = binding.query_config(M, N, K, **opts)
 
-    def gemm(a_, b_):
-        if forced:
-            return binding.gemm_tn_f16_ex(a_, b_, out=d, stream=stream, **opts)
-        return binding.gemm_tn_f16(a_, b_, out=d, stream=stream)
+    # Operand copies for the timed launches: launch i uses copy i % R, and the R
+    # copies together span at least 3 x L2, so every launch reads operands that
+    # the launches in between have evicted from L2 (inputs larger than L2).
+    per_copy = int(alg_bytes)
+    R = max(2, -(-3 * l2 // per_copy)) if args.timing == "rotate" else 1
+    a_all = torch.empty((R, M, K), dtype=torch.float16, device=dev)
+    b_all = torch.empty((R, N, K), dtype=torch.float16, device=dev)
+    d_all = torch.empty((R, M, N), dtype=torch.float16, device=dev)
+    a_all.copy_(a.unsqueeze(0).expand(R, M, K))
+    b_all.copy_(b.unsqueeze(0).expand(R, N, K))
+    del a, b
 
-    for _ in range(args.warmup):
-        gemm(a, b)
+    def gemm(a_, b_, d_):
+        if forced:
+            return binding.gemm_tn_f16_ex(a_, b_, out=d_, stream=stream, **opts)
+        return binding.gemm_tn_f16(a_, b_, out=d_, stream=stream)
+
+    def launch(i):
+        r = i % R
+        gemm(a_all[r], b_all[r], d_all[r])
+
+    for i in range(args.warmup):
+        launch(i)
     torch.cuda.synchronize(dev)
     status, raw = binding.get_device_error(stream)
     if status != 0:
         raise SystemExit(f"device error after warm-up: {raw:#x}")
 
+    # The rotated launches are replayed from CUDA graphs (one graph of R
+    # launches, one of the K mod R remainder), so the host's per-call Python
+    # and ctypes overhead does not starve the GPU on small shapes.
+    graphs = None
+    if args.timing == "rotate" and not args.no_graphs:
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+
+        def capture(n):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                cap = torch.cuda.current_stream(dev)
+                for i in range(n):
+                    r = i % R
+                    if forced:
+                        binding.gemm_tn_f16_ex(a_all[r], b_all[r], out=d_all[r], stream=cap, **opts)
+                    else:
+                        binding.gemm_tn_f16(a_all[r], b_all[r], out=d_all[r], stream=cap)
+            return g
+
+        graphs = (capture(R), capture(args.steps % R) if args.steps % R else None)
+        stream.wait_stream(side)
+        graphs[0].replay()                      # one untimed replay
+        torch.cuda.synchronize(dev)
+
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    clean = torch.zeros(2 * l2 // 4, dtype=torch.int32, device=dev)
+    sleep_cycles = int(args.launch_slack_us * 2.0e3)   # ~2 GHz SM clock
+
+    def isolated_launches(n, read_clean):
+        """Per-launch event pairs, each after an L2 flush (2 x L2 bytes
+        written, then optionally a clean buffer read) and a device sleep so the
+        launch is enqueued before its start event.  Each launch then also
+        carries the ~4-5 us event-to-kernel latency of an isolated launch."""
+        st = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        en = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for i in range(n):
+            flush.zero_()
+            if read_clean:
+                clean.sum()
+            if sleep_cycles:
+                torch.cuda._sleep(sleep_cycles)
+            st[i].record(stream)
+            gemm(a_all[0], b_all[0], d_all[0])
+            en[i].record(stream)
+        torch.cuda.synchronize(dev)
+        return [x.elapsed_time(y) for x, y in zip(st, en)]
+
     clocks = ClockSampler(local)
     clocks.start()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
     wall0 = time.perf_counter()
-    for i in range(args.steps):
-        flush.zero_()                           # evict A, B, D from L2 (not timed)
-        if clean is not None:
-            clean.sum()                         # replace the dirty flush lines with clean ones
-        if sleep_cycles:
-            # keep the GPU busy while the host enqueues the timed launch, so the
-            # start event does not wait on host-side launch overhead
-            torch.cuda._sleep(sleep_cycles)
-        starts[i].record(stream)
-        gemm(a, b)
-        ends[i].record(stream)
-    torch.cuda.synchronize(dev)
+    if args.timing == "rotate":
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        if graphs is not None:
+            g_full, g_rem = graphs
+            t_start.record(stream)
+            for _ in range(args.steps // R):
+                g_full.replay()
+            if g_rem is not None:
+                g_rem.replay()
+            t_end.record(stream)
+        else:
+            t_start.record(stream)
+            for i in range(args.steps):
+                launch(i)
+            t_end.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = t_start.elapsed_time(t_end) / args.steps
+        launches_ms = None
+    else:
+        launches_ms = isolated_launches(args.steps, True)
+        ms = statistics.mean(launches_ms)
     wall = time.perf_counter() - wall0
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
-    launches_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    ms = statistics.mean(launches_ms)
-    # the same launches after a write-only flush (dirty flush lines left in L2)
-    alt_ms = None
-    if clean is not None and args.alt_steps > 0:
-        n_alt = min(args.steps, args.alt_steps)
-        s_alt = [torch.cuda.Event(enable_timing=True) for _ in range(n_alt)]
-        e_alt = [torch.cuda.Event(enable_timing=True) for _ in range(n_alt)]
-        for i in range(n_alt):
-            flush.zero_()
-            if sleep_cycles:
-                torch.cuda._sleep(sleep_cycles)
-            s_alt[i].record(stream)
-            gemm(a, b)
-            e_alt[i].record(stream)
-        torch.cuda.synchronize(dev)
-        alt_ms = statistics.mean([x.elapsed_time(y) for x, y in zip(s_alt, e_alt)])
+    iso = None
+    if args.alt_steps > 0:
+        n_iso = min(args.steps, args.alt_steps)
+        iso_clean = isolated_launches(n_iso, True)
+        iso_dirty = isolated_launches(n_iso, False)
+        iso = {"steps": n_iso, "mean_ms_clean_flush": statistics.mean(iso_clean),
+               "median_ms_clean_flush": statistics.median(iso_clean),
+               "mean_ms_write_only_flush": statistics.mean(iso_dirty),
+               "note": "per-launch event pairs after an L2 flush; includes the isolated "
+                       "launch latency (an empty kernel measures ~4.5 us this way)"}
     if world > 1:
         t = torch.tensor([ms], dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -309,6 +372,7 @@ def run_gpu(args, tag):
     status, raw = binding.get_device_error(stream)
     if status != 0:
         raise SystemExit(f"device error in timed region: {raw:#x}")
+    d = d_all[0]
 
     # end to end from pinned host buffers through the public API
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
@@ -322,7 +386,7 @@ def run_gpu(args, tag):
     for _ in range(e2e_steps):
         a_e = a_host.to(dev, non_blocking=True)
         b_e = b_host.to(dev, non_blocking=True)
-        gemm(a_e, b_e)
+        gemm(a_e, b_e, d)
         d_host.copy_(d, non_blocking=True)
     e_end.record(stream)
     torch.cuda.synchronize(dev)
@@ -344,10 +408,20 @@ def run_gpu(args, tag):
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_source": f"{peak_src} hbm_gbs (copy bandwidth)"}
     else:
-        peak = float(peaks["bf16_tflops"])
+        # back-to-back launches run at the power cap: the sustained peak applies;
+        # a launch timed alone compares with the burst peak
+        sustained = args.timing == "rotate"
+        key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+        peak = float(peaks.get(key, peaks["bf16_tflops"]))
         roof = {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
                 "frac": tflops / peak,
-                "peak_source": f"{peak_src} bf16_tflops (burst) x fp16:bf16 nominal rate 1:1"}
+                "frac_of_burst_peak": tflops / float(peaks["bf16_tflops"]),
+                "peak_source": f"{peak_src} {key} ({'sustained, the timed region is a long run of '
+                               'back-to-back launches' if sustained else 'burst'}) x fp16:bf16 "
+                               f"nominal rate 1:1"}
+        if iso:
+            iso["tflops_clean_flush"] = flops / (iso["mean_ms_clean_flush"] * 1e-3) / 1e12
+            iso["frac_of_burst_peak"] = iso["tflops_clean_flush"] / float(peaks["bf16_tflops"])
     roof["kernel"] = KERNEL
     roof["traffic"] = recorded_traffic(tag)
     roof["alg_bytes_per_launch"] = alg_bytes
@@ -358,18 +432,23 @@ def run_gpu(args, tag):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
             "data": "synthetic (seeded splitmix64, fp16-rounded)",
             "config": workload_config(tag, spec, {
-                "l2": ("flushed before every timed launch: 2 x L2 bytes written" +
-                       (", then 2 x L2 bytes of a clean buffer read" if clean is not None else "") +
-                       ", outside the launch's event pair"),
-                "launch_slack_us": args.launch_slack_us,
+                "l2": (f"inputs larger than L2: {R} copies of A, B, D ({R * per_copy >> 20} MiB "
+                       f"> 3 x L2) cycled, launch i using copy i % {R}; one event pair around "
+                       f"the {args.steps} back-to-back launches" +
+                       (" (replayed from CUDA graphs)" if graphs is not None else "")
+                       if args.timing == "rotate" else
+                       "flushed before every timed launch: 2 x L2 bytes written, then 2 x L2 "
+                       "bytes of a clean buffer read, outside the launch's event pair"),
+                "timing": args.timing,
                 "path": ["auto", "square", "skinny", "pair"][cfg["path"]], "bm": cfg["bm"],
                 "bn": cfg["bn"], "bk": cfg["bk"], "kstage": cfg["kstage"], "ctas": cfg["ctas"],
-                "tiles": cfg["tiles"], "forced": forced}),
-            "launch_ms": {"mean": ms, "median": statistics.median(launches_ms),
-                          "p10": float(np.percentile(launches_ms, 10)),
-                          "p90": float(np.percentile(launches_ms, 90))},
+                "tiles": cfg["tiles"], "katoms": cfg["katoms"], "forced": forced}),
+            "launch_ms": ({"mean": ms, "median": statistics.median(launches_ms),
+                           "p10": float(np.percentile(launches_ms, 10)),
+                           "p90": float(np.percentile(launches_ms, 90))}
+                          if launches_ms else {"mean": ms}),
+            "launch_ms_isolated": iso,
             "roofline": roof,
-            "launch_ms_write_only_flush": alt_ms,
             "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                     "h2d_bytes_per_step": 2 * (M * K + N * K), "d2h_bytes_per_step": 2 * M * N,
                     "ms_per_step": e2e_ms, "steps": e2e_steps},
@@ -398,11 +477,16 @@ def main():
     ap.add_argument("--reference-budget", type=float, default=90.0,
                     help="target wall seconds for the whole --impl reference run")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
-    ap.add_argument("--flush", choices=["write", "write+read"], default="write+read",
-                    help="L2 flush before each timed launch: write 2 x L2 bytes, optionally "
-                         "followed by reading a clean buffer of that size")
+    ap.add_argument("--timing", choices=["rotate", "flush"], default="rotate",
+                    help="rotate: back-to-back launches over operand copies spanning > 3 x L2 "
+                         "(one event pair); flush: per-launch event pairs after an L2 flush")
     ap.add_argument("--alt-steps", type=int, default=100,
-                    help="extra launches timed after a write-only flush (reported, not the value)")
+                    help="extra isolated launches (flush + per-launch events), reported beside "
+                         "the value")
+    ap.add_argument("--katoms", type=int, default=0, help="diagnostics: force K slices per stage")
+    ap.add_argument("--group-m", type=int, default=0, help="diagnostics: rasterisation group")
+    ap.add_argument("--no-graphs", action="store_true",
+                    help="launch the rotated steps one by one instead of replaying CUDA graphs")
     ap.add_argument("--launch-slack-us", type=float, default=100.0,
                     help="device-side sleep before each start event (outside the timed pair)")
     ap.add_argument("--path", choices=["auto", "square", "skinny", "pair"], default="auto",

@@ -80,6 +80,8 @@ typedef struct {
   int inject;          /* test hook: 1 = the producer announces its first stage
                           but never loads it, so the consumers' waits run out;
                           the kernel then reports GEMM_ERR_TIMEOUT and exits   */
+  int katoms;          /* 64-wide K slices per ring stage: 0 = choose, 1 or 2 (a
+                          stage of 2 halves the per-byte barrier and commit work) */
 } gemm_options_t;
 
 /* gemm_tn_f16 with an explicit configuration (sweeps, tests).  Same
@@ -93,6 +95,7 @@ int gemm_tn_f16_ex(void* D, const void* A, const void* B, int64_t M, int64_t N, 
 typedef struct {
   int path, bm, bn, bk, kstage, ctas, group_m, tiles;
   int smem_bytes, tmem_cols;
+  int katoms;          /* bk = 64 * katoms */
 } gemm_config_t;
 int gemm_query_config(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt,
                       gemm_config_t* out);

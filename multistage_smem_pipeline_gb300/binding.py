@@ -31,12 +31,12 @@ EXPORTED = ("gemm_tn_f16", "gemm_tn_f16_ex", "gemm_query_config", "gemm_get_devi
 class GemmOptions(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("bn", ctypes.c_int), ("kstage", ctypes.c_int),
                 ("max_ctas", ctypes.c_int), ("group_m", ctypes.c_int),
-                ("timeout_ns", ctypes.c_uint64), ("inject", ctypes.c_int)]
+                ("timeout_ns", ctypes.c_uint64), ("inject", ctypes.c_int), ("katoms", ctypes.c_int)]
 
 
 class GemmConfig(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in ("path", "bm", "bn", "bk", "kstage", "ctas", "group_m",
-                                            "tiles", "smem_bytes", "tmem_cols")]
+                                            "tiles", "smem_bytes", "tmem_cols", "katoms")]
 
 
 class GemmError(RuntimeError):
@@ -89,9 +89,10 @@ def _stream_handle(stream) -> int:
     return int(s.cuda_stream)
 
 
-def _options(path=0, bn=0, kstage=0, max_ctas=0, group_m=0, timeout_ns=0, inject=0) -> GemmOptions:
+def _options(path=0, bn=0, kstage=0, max_ctas=0, group_m=0, timeout_ns=0, inject=0,
+             katoms=0) -> GemmOptions:
     return GemmOptions(int(path), int(bn), int(kstage), int(max_ctas), int(group_m),
-                       int(timeout_ns), int(inject))
+                       int(timeout_ns), int(inject), int(katoms))
 
 
 def _check_operands(a: torch.Tensor, b: torch.Tensor, out):
@@ -127,7 +128,8 @@ def gemm_tn_f16(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = Non
 
 def gemm_tn_f16_ex(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = None, stream=None,
                    **opts) -> torch.Tensor:
-    """gemm_tn_f16 with explicit options (path, bn, kstage, max_ctas, group_m, timeout_ns, inject)."""
+    """gemm_tn_f16 with explicit options (path, bn, kstage, max_ctas, group_m, timeout_ns,
+    inject, katoms)."""
     M, N, K, out = _check_operands(a, b, out)
     o = _options(**opts)
     with torch.cuda.device(a.device):

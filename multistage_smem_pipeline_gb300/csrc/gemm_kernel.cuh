@@ -100,14 +100,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmD);
   }
   __syncwarp();  // reconverge warp 0 before the aligned CTA barrier
-  if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), p.tmem_cols);
-    tmem_relinquish();
+  __syncthreads();  // barriers initialised: the producer may start loading at once
+  uint32_t tmem_base = 0;
+  if (warp != 0) {
+    // TMEM is needed only by the MMA and epilogue warps (1-5); they meet on
+    // named barrier 1 while the producer already streams the first stages.
+    if (warp == 1) {
+      tmem_alloc(smem_u32(tmem_slot), p.tmem_cols);
+      tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    named_barrier_sync(1, kThreads - 32);
+    tc_fence_after_sync();
+    tmem_base = *tmem_slot;
   }
-  tc_fence_before_sync();
-  __syncthreads();
-  tc_fence_after_sync();
-  const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -129,17 +135,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const uint32_t a_dst = base + L.ring + stage * p.stage_bytes;
-          const uint32_t b_dst = a_dst + kABytes;
+          const uint32_t b_dst = a_dst + p.katoms * kABytes;
           mbar_arrive_expect_tx(full_bar(stage), p.stage_bytes);
           if (!(p.inject == 1 && issued == 0)) {
-            if (p.l2_hints & 2u)
-              tma_load_2d_hint(a_dst, &tmA, full_bar(stage), kb * kBK, mb * kBM, pol_a);
-            else
-              tma_load_2d(a_dst, &tmA, full_bar(stage), kb * kBK, mb * kBM);
-            if (p.l2_hints & 1u)
-              tma_load_2d_hint(b_dst, &tmB, full_bar(stage), kb * kBK, nb * p.bn, pol_b);
-            else
-              tma_load_2d(b_dst, &tmB, full_bar(stage), kb * kBK, nb * p.bn);
+            for (int at = 0; at < p.katoms; ++at) {
+              const int x = (kb * p.katoms + at) * kBK;  // past K: the box reads zeros
+              const uint32_t ad = a_dst + at * kABytes, bd = b_dst + at * p.b_atom_bytes;
+              if (p.l2_hints & 2u)
+                tma_load_2d_hint(ad, &tmA, full_bar(stage), x, mb * kBM, pol_a);
+              else
+                tma_load_2d(ad, &tmA, full_bar(stage), x, mb * kBM);
+              if (p.l2_hints & 1u)
+                tma_load_2d_hint(bd, &tmB, full_bar(stage), x, nb * p.bn, pol_b);
+              else
+                tma_load_2d(bd, &tmB, full_bar(stage), x, nb * p.bn);
+            }
           }
           ++issued;
           if (++stage == S) {
@@ -176,13 +186,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after_sync();
           const uint32_t a_src = base + L.ring + stage * p.stage_bytes;
-          const uint64_t a_desc = sw128_kmajor_desc(a_src);
-          const uint64_t b_desc = sw128_kmajor_desc(a_src + kABytes);
+          const uint32_t b_src = a_src + p.katoms * kABytes;
+          for (int at = 0; at < p.katoms; ++at) {
+            const uint64_t a_desc = sw128_kmajor_desc(a_src + at * kABytes);
+            const uint64_t b_desc = sw128_kmajor_desc(b_src + at * p.b_atom_bytes);
 #pragma unroll
-          for (int k = 0; k < kBK / kUmmaK; ++k) {
-            // +32 bytes along K inside the 128-byte swizzle row = +2 in the
-            // descriptor's address field (16-byte units)
-            umma_f16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, p.idesc, (i | k) != 0);
+            for (int k = 0; k < kBK / kUmmaK; ++k) {
+              // +32 bytes along K inside the 128-byte swizzle row = +2 in the
+              // descriptor's address field (16-byte units)
+              umma_f16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, p.idesc, (i | at | k) != 0);
+            }
           }
           umma_commit(empty_bar(stage));  // frees the stage once these MMAs have read it
           if (++stage == S) {

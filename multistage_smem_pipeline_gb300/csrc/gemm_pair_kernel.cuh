@@ -114,18 +114,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const uint32_t a_dst = base + L.ring + stage * p.stage_bytes;
-          const uint32_t b_dst = a_dst + kABytes;
+          const uint32_t b_dst = a_dst + p.katoms * kABytes;
           const uint32_t leader_full = mapa_shared(full_bar(stage), 0);
           if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2u * p.stage_bytes);
           if (!(p.inject == 1 && issued == 0 && rank == 0)) {
-            if (p.l2_hints & 2u)
-              tma_load_2d_pair_hint(a_dst, &tmA, leader_full, kb * kBK, a_row, pol_a);
-            else
-              tma_load_2d_pair(a_dst, &tmA, leader_full, kb * kBK, a_row);
-            if (p.l2_hints & 1u)
-              tma_load_2d_pair_hint(b_dst, &tmB, leader_full, kb * kBK, b_row, pol_b);
-            else
-              tma_load_2d_pair(b_dst, &tmB, leader_full, kb * kBK, b_row);
+            for (int at = 0; at < p.katoms; ++at) {
+              const int x = (kb * p.katoms + at) * kBK;  // past K: the box reads zeros
+              const uint32_t ad = a_dst + at * kABytes, bd = b_dst + at * p.b_atom_bytes;
+              if (p.l2_hints & 2u)
+                tma_load_2d_pair_hint(ad, &tmA, leader_full, x, a_row, pol_a);
+              else
+                tma_load_2d_pair(ad, &tmA, leader_full, x, a_row);
+              if (p.l2_hints & 1u)
+                tma_load_2d_pair_hint(bd, &tmB, leader_full, x, b_row, pol_b);
+              else
+                tma_load_2d_pair(bd, &tmB, leader_full, x, b_row);
+            }
           }
           ++issued;
           if (++stage == S) {
@@ -162,11 +166,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after_sync();
           const uint32_t a_src = base + L.ring + stage * p.stage_bytes;
-          const uint64_t a_desc = sw128_kmajor_desc(a_src);
-          const uint64_t b_desc = sw128_kmajor_desc(a_src + kABytes);
+          const uint32_t b_src = a_src + p.katoms * kABytes;
+          for (int at = 0; at < p.katoms; ++at) {
+            const uint64_t a_desc = sw128_kmajor_desc(a_src + at * kABytes);
+            const uint64_t b_desc = sw128_kmajor_desc(b_src + at * p.b_atom_bytes);
 #pragma unroll
-          for (int k = 0; k < kBK / kUmmaK; ++k)
-            umma_f16_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, p.idesc, (i | k) != 0);
+            for (int k = 0; k < kBK / kUmmaK; ++k)
+              umma_f16_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, p.idesc, (i | at | k) != 0);
+          }
           umma_commit_pair_mc(empty_bar(stage), 0x3);
           if (++stage == S) {
             stage = 0;

@@ -32,7 +32,9 @@ struct GemmParams {
   int32_t group_m;       // m-blocks per rasterisation group
   uint32_t idesc;        // tcgen05 instruction descriptor
   uint32_t tmem_cols;    // allocated TMEM columns (power of two >= 2*bn)
-  uint32_t stage_bytes;  // kABytes + bn * 128
+  uint32_t stage_bytes;  // katoms * (kABytes + b_atom_bytes)
+  uint32_t b_atom_bytes; // B rows per CTA x 128 B: one 64-wide K atom of B
+  int32_t katoms;        // 64-wide K atoms per stage (1 or 2); a k-block is 64 * katoms wide
   uint32_t l2_hints;     // bit 0: stream B with evict-first; bit 1: keep A with evict-last
   uint64_t timeout_ns;
   int32_t inject;

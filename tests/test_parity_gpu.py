@@ -95,6 +95,28 @@ def test_every_ring_depth_and_wrap(lib, gpu, path, bn):
             _check(got, a, b)
 
 
+@pytest.mark.parametrize("path,bn", [(SQUARE, 256), (SQUARE, 96), (PAIR, 256), (PAIR, 128)])
+def test_two_k_slices_per_stage(lib, gpu, path, bn):
+    # katoms = 2: each ring stage holds two 64-wide K slices; K values put the
+    # tail in the first or the second slice, or leave the second slice entirely
+    # past K (its loads read zeros), and the ring wraps at every depth
+    deepest = lib.query_config(384, 520, 4096, bn=bn, path=path, katoms=2)["kstage"]
+    for ks in range(2, deepest + 1):
+        for K in (64, 120, 128, 136, 64 * 2 * ks + 64, 64 * 2 * (ks + 1) + 8):
+            a = synthetic.uniform_pm1(K + ks, (384, K))
+            b = synthetic.uniform_pm1(K + ks + 1, (520, K))
+            got = _run(lib, a, b, gpu, bn=bn, kstage=ks, katoms=2, path=path,
+                       max_ctas=2 if path == PAIR else 1)
+            _check(got, a, b)
+
+
+def test_two_k_slices_ternary_is_bit_exact(lib, gpu):
+    a, b, spec = synthetic.workload("c2")
+    for path in (SQUARE, PAIR):
+        got = _run(lib, a, b, gpu, katoms=2, path=path)
+        assert np.array_equal(got, oracle.gemm_tn(a, b))
+
+
 @pytest.mark.parametrize("path", [SQUARE, PAIR])
 @pytest.mark.parametrize("ctas,group_m", [(2, 1), (6, 2), (10, 16), (0, 3)])
 def test_persistent_schedules(lib, gpu, ctas, group_m, path):

@@ -112,7 +112,8 @@ def test_valid_call_without_a_device_reports_cuda_error(binding):
 
 def test_query_config_plans(binding):
     c = binding.query_config(8192, 8192, 8192)
-    assert c["path"] == binding.PATH_PAIR and c["bm"] == 256 and c["bk"] == 64
+    assert c["path"] == binding.PATH_PAIR and c["bm"] == 256 and c["bk"] == 64 * c["katoms"]
+    assert c["katoms"] in (1, 2)
     assert c["ctas"] % 2 == 0
     assert c["bn"] % 32 == 0 and 32 <= c["bn"] <= 256
     assert c["kstage"] >= 2 and c["smem_bytes"] <= 232448
@@ -120,19 +121,27 @@ def test_query_config_plans(binding):
     assert c["tmem_cols"] & (c["tmem_cols"] - 1) == 0
     s = binding.query_config(128, 14336, 4096)
     assert s["path"] == binding.PATH_SKINNY and s["tiles"] <= s["ctas"] * 2
-    # every explicit (path, bn, kstage) that is accepted fits the shared-memory budget
+    # every explicit (path, bn, katoms, kstage) that is accepted fits the shared-memory budget
     for path in (binding.PATH_SQUARE, binding.PATH_PAIR):
-        for bn in range(32, 257, 32):
-            deepest = binding.query_config(1024, 1024, 1024, path=path, bn=bn)["kstage"]
-            for ks in range(2, deepest + 1):
-                cc = binding.query_config(1024, 1024, 1024, path=path, bn=bn, kstage=ks)
-                assert cc["smem_bytes"] <= 232448 and cc["kstage"] == ks and cc["path"] == path
-                assert cc["bm"] == (256 if path == binding.PATH_PAIR else 128)
-            with pytest.raises(binding.GemmError):
-                binding.query_config(1024, 1024, 1024, path=path, bn=bn, kstage=deepest + 1)
+        for katoms in (1, 2):
+            for bn in range(32, 257, 32):
+                q = dict(path=path, bn=bn, katoms=katoms)
+                deepest = binding.query_config(1024, 1024, 1024, **q)["kstage"]
+                for ks in range(2, deepest + 1):
+                    cc = binding.query_config(1024, 1024, 1024, kstage=ks, **q)
+                    assert cc["smem_bytes"] <= 232448 and cc["kstage"] == ks
+                    assert cc["path"] == path and cc["katoms"] == katoms
+                    assert cc["bm"] == (256 if path == binding.PATH_PAIR else 128)
+                with pytest.raises(binding.GemmError):
+                    binding.query_config(1024, 1024, 1024, kstage=deepest + 1, **q)
     # a pair stage holds half of B, so the pair ring is deeper at the same width
-    assert binding.query_config(4096, 4096, 4096, path=binding.PATH_PAIR, bn=256)["kstage"] > \
-        binding.query_config(4096, 4096, 4096, path=binding.PATH_SQUARE, bn=256)["kstage"]
+    assert binding.query_config(4096, 4096, 4096, path=binding.PATH_PAIR, bn=256, katoms=1)[
+        "kstage"] > binding.query_config(4096, 4096, 4096, path=binding.PATH_SQUARE, bn=256,
+                                         katoms=1)["kstage"]
+    # two K slices per stage only where the ring keeps at least 3 stages
+    for shape in [(8192, 8192, 8192), (128, 14336, 4096), (256, 256, 256)]:
+        cc = binding.query_config(*shape)
+        assert cc["katoms"] == 1 or cc["kstage"] >= 3
 
 
 def test_status_strings(binding):

@@ -243,7 +243,8 @@ def run_gpu(args, tag):
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     stream = torch.cuda.current_stream(dev)
     opts = {"path": ["auto", "square", "skinny", "pair"].index(args.path), "bn": args.bn,
-            "kstage": args.kstage, "katoms": args.katoms, "group_m": args.group_m}
+            "kstage": args.kstage, "katoms": args.katoms, "group_m": args.group_m,
+            "epi_warps": args.epi_warps}
     forced = any(opts.values())
     cfg = binding.query_config(M, N, K, **opts)
 
@@ -401,7 +402,9 @@ def run_gpu(args, tag):
 
     peaks, peak_src = load_peaks()
     tflops = flops / (ms * 1e-3) / 1e12
-    hbm_bound = tag == "c5"
+    # the roofline that binds: arithmetic intensity against the measured ridge point
+    ridge = float(peaks["bf16_tflops"]) * 1e12 / (float(peaks["hbm_gbs"]) * 1e9)
+    hbm_bound = flops / alg_bytes < ridge
     if hbm_bound:
         achieved = alg_bytes / (ms * 1e-3) / 1e9
         peak = float(peaks["hbm_gbs"])
@@ -442,7 +445,8 @@ def run_gpu(args, tag):
                 "timing": args.timing,
                 "path": ["auto", "square", "skinny", "pair"][cfg["path"]], "bm": cfg["bm"],
                 "bn": cfg["bn"], "bk": cfg["bk"], "kstage": cfg["kstage"], "ctas": cfg["ctas"],
-                "tiles": cfg["tiles"], "katoms": cfg["katoms"], "forced": forced}),
+                "tiles": cfg["tiles"], "katoms": cfg["katoms"], "epi_warps": cfg["epi_warps"],
+                "forced": forced}),
             "launch_ms": ({"mean": ms, "median": statistics.median(launches_ms),
                            "p10": float(np.percentile(launches_ms, 10)),
                            "p90": float(np.percentile(launches_ms, 90))}
@@ -485,6 +489,7 @@ def main():
                          "the value")
     ap.add_argument("--katoms", type=int, default=0, help="diagnostics: force K slices per stage")
     ap.add_argument("--group-m", type=int, default=0, help="diagnostics: rasterisation group")
+    ap.add_argument("--epi-warps", type=int, default=0, help="diagnostics: epilogue warps (4, 8)")
     ap.add_argument("--no-graphs", action="store_true",
                     help="launch the rotated steps one by one instead of replaying CUDA graphs")
     ap.add_argument("--launch-slack-us", type=float, default=100.0,

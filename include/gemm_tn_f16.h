@@ -82,6 +82,8 @@ typedef struct {
                           the kernel then reports GEMM_ERR_TIMEOUT and exits   */
   int katoms;          /* 64-wide K slices per ring stage: 0 = choose, 1 or 2 (a
                           stage of 2 halves the per-byte barrier and commit work) */
+  int epi_warps;       /* epilogue warps per CTA: 0 = choose, 4 or 8 (8 doubles the
+                          TMEM -> global drain rate, for short k loops) */
 } gemm_options_t;
 
 /* gemm_tn_f16 with an explicit configuration (sweeps, tests).  Same
@@ -96,6 +98,7 @@ typedef struct {
   int path, bm, bn, bk, kstage, ctas, group_m, tiles;
   int smem_bytes, tmem_cols;
   int katoms;          /* bk = 64 * katoms */
+  int epi_warps;       /* threads per CTA = 64 + 32 * epi_warps */
 } gemm_config_t;
 int gemm_query_config(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt,
                       gemm_config_t* out);

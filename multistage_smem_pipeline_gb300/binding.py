@@ -31,12 +31,14 @@ EXPORTED = ("gemm_tn_f16", "gemm_tn_f16_ex", "gemm_query_config", "gemm_get_devi
 class GemmOptions(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("bn", ctypes.c_int), ("kstage", ctypes.c_int),
                 ("max_ctas", ctypes.c_int), ("group_m", ctypes.c_int),
-                ("timeout_ns", ctypes.c_uint64), ("inject", ctypes.c_int), ("katoms", ctypes.c_int)]
+                ("timeout_ns", ctypes.c_uint64), ("inject", ctypes.c_int), ("katoms", ctypes.c_int),
+                ("epi_warps", ctypes.c_int)]
 
 
 class GemmConfig(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in ("path", "bm", "bn", "bk", "kstage", "ctas", "group_m",
-                                            "tiles", "smem_bytes", "tmem_cols", "katoms")]
+                                            "tiles", "smem_bytes", "tmem_cols", "katoms",
+                                            "epi_warps")]
 
 
 class GemmError(RuntimeError):
@@ -90,9 +92,9 @@ def _stream_handle(stream) -> int:
 
 
 def _options(path=0, bn=0, kstage=0, max_ctas=0, group_m=0, timeout_ns=0, inject=0,
-             katoms=0) -> GemmOptions:
+             katoms=0, epi_warps=0) -> GemmOptions:
     return GemmOptions(int(path), int(bn), int(kstage), int(max_ctas), int(group_m),
-                       int(timeout_ns), int(inject), int(katoms))
+                       int(timeout_ns), int(inject), int(katoms), int(epi_warps))
 
 
 def _check_operands(a: torch.Tensor, b: torch.Tensor, out):
@@ -129,7 +131,7 @@ def gemm_tn_f16(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = Non
 def gemm_tn_f16_ex(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = None, stream=None,
                    **opts) -> torch.Tensor:
     """gemm_tn_f16 with explicit options (path, bn, kstage, max_ctas, group_m, timeout_ns,
-    inject, katoms)."""
+    inject, katoms, epi_warps)."""
     M, N, K, out = _check_operands(a, b, out)
     o = _options(**opts)
     with torch.cuda.device(a.device):

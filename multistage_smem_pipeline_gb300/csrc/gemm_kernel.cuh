@@ -5,9 +5,11 @@
 //                          (BN x 64) k-blocks into a `stages`-deep ring;
 //   warp 1, one thread  -- MMA issuer: 4 x tcgen05.mma (K = 16 each) per
 //                          k-block into an fp32 accumulator in TMEM;
-//   warps 2-5           -- epilogue: TMEM -> registers -> fp16 -> swizzled
-//                          shared memory -> TMA store, while the MMA thread
-//                          already fills the second TMEM accumulator.
+//   warps 2..          -- epilogue (4 or 8 warps): TMEM -> registers -> fp16 ->
+//                          swizzled shared memory -> TMA store, while the MMA
+//                          thread already fills the second TMEM accumulator;
+//                          with 8 warps two share each TMEM lane quadrant and
+//                          take alternate 32-column chunks.
 //
 // This is the multistage pipeline of "cute(9) multistage_gemm" (sections 4-6:
 // a ring of kStage K-tiles, a prologue that runs ahead, a mainloop that
@@ -59,7 +61,8 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uin
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+template <int kEpiWarps>
+__global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
     gemm_tn_f16_persistent(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
                            const __grid_constant__ CUtensorMap tmD, const GemmParams p) {
@@ -67,7 +70,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* const smem = smem_raw + (base - raw);
-  const SmemLayout L = SmemLayout::make(p.stages, p.stage_bytes);
+  constexpr int kThreads = threads_for(kEpiWarps);
+  constexpr int kChunkStride = kEpiWarps / 4;  // warps sharing a TMEM lane quadrant
+  const SmemLayout L = SmemLayout::make(p.stages, p.stage_bytes, kEpiWarps);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -103,7 +108,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();  // barriers initialised: the producer may start loading at once
   uint32_t tmem_base = 0;
   if (warp != 0) {
-    // TMEM is needed only by the MMA and epilogue warps (1-5); they meet on
+    // TMEM is needed only by the MMA and epilogue warps (1..); they meet on
     // named barrier 1 while the producer already streams the first stages.
     if (warp == 1) {
       tmem_alloc(smem_u32(tmem_slot), p.tmem_cols);
@@ -216,7 +221,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    // epilogue warps: lane quadrant warp % 4 (the quadrant a warp may access
+    // in TMEM); with 8 warps, each takes every other 32-column chunk of it
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
     const uint32_t my_bufs = base + L.epi + (warp - 2) * kEpiBufs * kEpiChunkBytes;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -236,11 +244,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nchunks = (min(p.bn, p.N - n0) + kEpiCols - 1) / kEpiCols;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * p.bn);
-      for (int c = 0; c < nchunks && rows_live; ++c) {
+      const int last_c = last_epi_chunk(nchunks, half, kChunkStride);
+      for (int c = half; c <= last_c && rows_live; c += kChunkStride) {
         uint32_t r[32];
         tmem_ld_32x32b_x32(t_row + c * kEpiCols, r);
         tmem_ld_wait();
-        if (c == nchunks - 1) {  // accumulator fully read: hand it back to the MMA thread
+        if (c == last_c) {  // accumulator fully read: hand it back to the MMA thread
           tc_fence_before_sync();
           __syncwarp();
           if (lane == 0) mbar_arrive(tempty_bar(acc));
@@ -270,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ++chunk_seq;
       }
-      if (!rows_live) {  // this quadrant lies below M: nothing to store, release at once
+      if (!rows_live || last_c < 0) {  // nothing for this warp to store: release at once
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(tempty_bar(acc));

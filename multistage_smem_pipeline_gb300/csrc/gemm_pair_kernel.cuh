@@ -21,7 +21,7 @@
 //                would put a fence in the producer's loop;
 //   empty[s]     both CTAs, count 1: the pair MMA's commit, multicast;
 //   tfull[b]     both CTAs, count 1: commit after a tile's last k-block, multicast;
-//   tempty[b]    even CTA only, count 8: every epilogue warp of both CTAs;
+//   tempty[b]    even CTA only: one arrive per epilogue warp of both CTAs;
 //   drain        even CTA: final commit before TMEM is freed.
 // As in the single-CTA kernel, every wait is bounded and a timeout is
 // reported through the device error word.  On that path the odd CTA cannot
@@ -33,9 +33,8 @@
 
 namespace gb300 {
 
-constexpr int kPairEpiArrivals = 2 * kEpiWarps;
-
-__global__ void __launch_bounds__(kThreads, 1)
+template <int kEpiWarps>
+__global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
     gemm_tn_f16_pair(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmD, const GemmParams p) {
@@ -43,7 +42,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* const smem = smem_raw + (base - raw);
-  const SmemLayout L = SmemLayout::make(p.stages, p.stage_bytes);
+  constexpr int kThreads = threads_for(kEpiWarps);
+  constexpr int kChunkStride = kEpiWarps / 4;  // warps sharing a TMEM lane quadrant
+  const SmemLayout L = SmemLayout::make(p.stages, p.stage_bytes, kEpiWarps);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -68,7 +69,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), kPairEpiArrivals);
+      mbar_init(tempty_bar(b), 2 * kEpiWarps);  // every epilogue warp of both CTAs
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -192,7 +193,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
+    // epilogue warps: lane quadrant warp % 4 (the quadrant a warp may access
+    // in TMEM); with 8 warps, each takes every other 32-column chunk of it
     const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
     const uint32_t my_bufs = base + L.epi + (warp - 2) * kEpiBufs * kEpiChunkBytes;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -213,11 +217,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * p.bn);
       const uint32_t leader_tempty = mapa_shared(tempty_bar(acc), 0);
-      for (int c = 0; c < nchunks && rows_live; ++c) {
+      const int last_c = last_epi_chunk(nchunks, half, kChunkStride);
+      for (int c = half; c <= last_c && rows_live; c += kChunkStride) {
         uint32_t r[32];
         tmem_ld_32x32b_x32(t_row + c * kEpiCols, r);
         tmem_ld_wait();
-        if (c == nchunks - 1) {
+        if (c == last_c) {
           tc_fence_before_sync();
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(leader_tempty);
@@ -244,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ++chunk_seq;
       }
-      if (!rows_live) {
+      if (!rows_live || last_c < 0) {
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(leader_tempty);

@@ -89,8 +89,8 @@ uint32_t make_idesc(int m, int n) {
   return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 
-int stages_that_fit(uint32_t stage_bytes) {
-  const uint32_t fixed = kEpiWarps * kEpiBufs * kEpiChunkBytes + 16 + 1024;
+int stages_that_fit(uint32_t stage_bytes, int epi_warps) {
+  const uint32_t fixed = epi_warps * kEpiBufs * kEpiChunkBytes + 16 + 1024;
   int s = 2;
   while (s + 1 <= kMaxStages) {
     const uint32_t bars = 8u * (2 * (s + 1) + 5);
@@ -129,7 +129,8 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   if (opt) o = *opt;
   if (o.path < 0 || o.path > 3 || o.bn < 0 || o.bn > 256 || (o.bn % 32) != 0 || o.kstage < 0 ||
       o.kstage == 1 || o.kstage > kMaxStages || o.max_ctas < 0 || o.group_m < 0 || o.inject < 0 ||
-      o.inject > 1 || o.katoms < 0 || o.katoms > 2)
+      o.inject > 1 || o.katoms < 0 || o.katoms > 2 ||
+      (o.epi_warps != 0 && o.epi_warps != 4 && o.epi_warps != 8))
     return GEMM_ERR_INVALID_VALUE;
   if (o.path == GEMM_PATH_SKINNY && M > kBM) return GEMM_ERR_INVALID_VALUE;
   if (max_pairs < 1) max_pairs = std::max(1, sms / 2);
@@ -144,8 +145,13 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
     if (o.path != GEMM_PATH_AUTO) {
       const int want = (o.path == GEMM_PATH_SKINNY) ? GEMM_PATH_SQUARE : o.path;
       if (kind != want) continue;
-    } else if (kind == GEMM_PATH_PAIR && M <= kBM) {
-      continue;  // a pair tile would be at least half empty
+    } else if (kind == GEMM_PATH_PAIR && (M <= kBM || K <= 1024)) {
+      // M <= 128: a pair tile would be at least half empty.  K <= 1024: the
+      // k loop per tile is short, so the pair's per-tile costs (2-CTA
+      // handshakes, twice the TMEM drained per tile) outweigh its lower
+      // operand traffic per k-block (measured: 256^3, 1024^3 and 81920x256x256
+      // all faster on single-CTA tiles).
+      continue;
     }
     for (int cand = 256; cand >= 32; cand -= 32) {
       if (o.bn && cand != o.bn) continue;
@@ -170,14 +176,20 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   const int64_t num_n = (N + bn - 1) / bn;
   const int64_t tiles = num_m * num_n;
   if (tiles > INT_MAX) return GEMM_ERR_INVALID_VALUE;
+  // Eight epilogue warps drain a tile twice as fast; they pay off when the k
+  // loop per tile is short (the epilogue is then the critical path), four
+  // are enough -- and leave the MMA and producer warps their issue slots --
+  // when it is long.
+  const int epi_warps = o.epi_warps ? o.epi_warps : (K <= 1024 ? 8 : 4);
   // Two 64-wide K slices per stage halve the issuing threads' per-byte
   // barrier/commit work (measured: +12 % at 8192^3); used whenever the ring
   // still gets at least 3 stages.
   const int katoms =
-      o.katoms ? o.katoms : (stages_that_fit(stage_bytes_for(path, bn, 2)) >= 3 ? 2 : 1);
+      o.katoms ? o.katoms
+               : (stages_that_fit(stage_bytes_for(path, bn, 2), epi_warps) >= 3 ? 2 : 1);
   const int64_t num_k = (K + kBK * katoms - 1) / (kBK * katoms);
   const uint32_t stage_bytes = stage_bytes_for(path, bn, katoms);
-  const int fit = stages_that_fit(stage_bytes);
+  const int fit = stages_that_fit(stage_bytes, epi_warps);
   const int stages = o.kstage ? o.kstage : fit;
   if (stages > fit) return GEMM_ERR_INVALID_VALUE;
   int ctas;
@@ -190,7 +202,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
     if (o.max_ctas) ctas = std::min(ctas, o.max_ctas);
   }
   const int group_m = o.group_m ? o.group_m : (path == GEMM_PATH_PAIR ? 8 : 16);
-  const SmemLayout L = SmemLayout::make(stages, stage_bytes);
+  const SmemLayout L = SmemLayout::make(stages, stage_bytes, epi_warps);
 
   Plan pl;
   std::memset(&pl, 0, sizeof(pl));
@@ -199,6 +211,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   pl.cfg.bn = bn;
   pl.cfg.bk = kBK * katoms;
   pl.cfg.katoms = katoms;
+  pl.cfg.epi_warps = epi_warps;
   pl.cfg.kstage = stages;
   pl.cfg.ctas = ctas;
   pl.cfg.group_m = group_m;
@@ -222,6 +235,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   p.stage_bytes = stage_bytes;
   p.b_atom_bytes = b_atom_bytes_for(path, bn);
   p.katoms = katoms;
+  p.epi_warps = epi_warps;
   // One m-block: every tile reads the same rows of A (keep them in L2, stream
   // B through it once) and the k loops are rotated across tiles.
   p.l2_hints = (num_m == 1) ? 3u : 0u;
@@ -251,14 +265,19 @@ int prepare_device(DeviceState* st) {
   std::lock_guard<std::mutex> lk(g_mu);
   if (st->smem_attr == kMaxDynSmem && st->pair_smem_attr == kMaxDynSmem && st->max_pairs > 0)
     return GEMM_OK;
-  if (cudaFuncSetAttribute(gemm_tn_f16_persistent, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(gemm_tn_f16_persistent<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kMaxDynSmem) != cudaSuccess ||
-      cudaFuncSetAttribute(gemm_tn_f16_pair, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      cudaFuncSetAttribute(gemm_tn_f16_persistent<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kMaxDynSmem) != cudaSuccess ||
+      cudaFuncSetAttribute(gemm_tn_f16_pair<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kMaxDynSmem) != cudaSuccess ||
+      cudaFuncSetAttribute(gemm_tn_f16_pair<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kMaxDynSmem) != cudaSuccess) {
     cudaGetLastError();
     return GEMM_ERR_CUDA;
   }
   st->smem_attr = st->pair_smem_attr = kMaxDynSmem;
+  // co-resident 2-CTA clusters, for the larger of the two block sizes
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
   cudaLaunchAttribute attr[1];
@@ -267,12 +286,12 @@ int prepare_device(DeviceState* st) {
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(2 * (st->sm_count / 2), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(threads_for(8), 1, 1);
   cfg.dynamicSmemBytes = kMaxDynSmem;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&clusters, gemm_tn_f16_pair, &cfg) != cudaSuccess ||
+  if (cudaOccupancyMaxActiveClusters(&clusters, gemm_tn_f16_pair<8>, &cfg) != cudaSuccess ||
       clusters < 1) {
     cudaGetLastError();
     clusters = st->sm_count / 2;
@@ -337,9 +356,14 @@ int run(void* D, const void* A, const void* B, int64_t M, int64_t N, int64_t K,
       encode_2d(&tmD, D, N, M, kEpiCols, 32, CU_TENSOR_MAP_SWIZZLE_64B) != GEMM_OK)
     return GEMM_ERR_INVALID_VALUE;
 
+  const int threads = threads_for(pl.cfg.epi_warps);
   if (!pair) {
-    gemm_tn_f16_persistent<<<pl.cfg.ctas, kThreads, pl.cfg.smem_bytes, stream>>>(tmA, tmB, tmD,
-                                                                                 pl.p);
+    if (pl.cfg.epi_warps == 8)
+      gemm_tn_f16_persistent<8><<<pl.cfg.ctas, threads, pl.cfg.smem_bytes, stream>>>(tmA, tmB, tmD,
+                                                                                   pl.p);
+    else
+      gemm_tn_f16_persistent<4><<<pl.cfg.ctas, threads, pl.cfg.smem_bytes, stream>>>(tmA, tmB, tmD,
+                                                                                   pl.p);
   } else {
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
@@ -349,12 +373,15 @@ int run(void* D, const void* A, const void* B, int64_t M, int64_t N, int64_t K,
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3(pl.cfg.ctas, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
     cfg.dynamicSmemBytes = pl.cfg.smem_bytes;
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, gemm_tn_f16_pair, tmA, tmB, tmD, pl.p) != cudaSuccess) {
+    const cudaError_t e = pl.cfg.epi_warps == 8
+                              ? cudaLaunchKernelEx(&cfg, gemm_tn_f16_pair<8>, tmA, tmB, tmD, pl.p)
+                              : cudaLaunchKernelEx(&cfg, gemm_tn_f16_pair<4>, tmA, tmB, tmD, pl.p);
+    if (e != cudaSuccess) {
       cudaGetLastError();
       return GEMM_ERR_LAUNCH;
     }

@@ -13,8 +13,10 @@ namespace gb300 {
 constexpr int kBM = 128;             // UMMA M: one TMEM lane per output row
 constexpr int kBK = 64;              // 64 fp16 = 128 B = one 128-byte swizzle row
 constexpr int kUmmaK = 16;           // K per tcgen05.mma (kind::f16)
-constexpr int kThreads = 192;        // 6 warps
-constexpr int kEpiWarps = 4;
+// Epilogue warps per CTA: 4 (one per TMEM lane quadrant) or 8 (two per
+// quadrant, taking alternate 32-column chunks).  The block is the producer
+// warp, the MMA warp and the epilogue warps.
+__host__ __device__ constexpr int threads_for(int epi_warps) { return 64 + 32 * epi_warps; }
 constexpr int kEpiBufs = 2;          // store staging buffers per epilogue warp
 constexpr int kEpiCols = 32;         // columns per epilogue chunk (one tcgen05.ld x32)
 constexpr uint32_t kEpiChunkBytes = 32 * kEpiCols * 2;  // 32 rows x 32 fp16
@@ -39,6 +41,7 @@ struct GemmParams {
   uint64_t timeout_ns;
   int32_t inject;
   int32_t k_rotate;      // 1: each tile starts its k loop at a tile-dependent k-block
+  int32_t epi_warps;     // epilogue warps (4 or 8); must match the launched kernel
 };
 
 // First k-block of tile t.  With rotation the tiles in flight start at
@@ -54,16 +57,23 @@ __device__ __forceinline__ int first_k_block(int t, const GemmParams& p) {
 // Shared-memory carve-up, offsets from the 1024-aligned base.
 struct SmemLayout {
   uint32_t ring, epi, bars, misc, total;
-  __host__ __device__ static SmemLayout make(int stages, uint32_t stage_bytes) {
+  __host__ __device__ static SmemLayout make(int stages, uint32_t stage_bytes, int epi_warps) {
     SmemLayout L;
     L.ring = 0;
     L.epi = stages * stage_bytes;
-    L.bars = L.epi + kEpiWarps * kEpiBufs * kEpiChunkBytes;
+    L.bars = L.epi + epi_warps * kEpiBufs * kEpiChunkBytes;
     L.misc = L.bars + 8 * (2 * stages + 5);
     L.total = L.misc + 16;
     return L;
   }
 };
+
+// Chunks of 32 columns handled by one epilogue warp: `half` in [0, stride)
+// picks every stride-th chunk; returns the last one (or -1 if none).
+__device__ __forceinline__ int last_epi_chunk(int nchunks, int half, int stride) {
+  const int top = nchunks - 1 - half;
+  return top < 0 ? -1 : nchunks - 1 - (top % stride);
+}
 
 // Bounded wait that ignores the abort flag: used while draining.
 __device__ __forceinline__ bool wait_timed(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {

@@ -9,7 +9,7 @@ s is mix(s + (i + 1) * 0x9E3779B97F4A7C15) with the published mixing
 constants; a uniform double in [0, 1) is its top 53 bits times 2^-53.  Normals
 use the Box-Muller transform on pairs of uniforms.
 
-Workloads (the five GEMM shapes the pages' pipeline is measured on, with the
+Workloads (the GEMM shapes the pipeline is measured and checked on, with the
 value distributions they are checked with):
 
 =====  =======================  ===========================================
@@ -20,6 +20,9 @@ c2     1024 x 1024 x 1024       uniform over {-1, 0, 1}
 c3     4096 x 4096 x 4096       N(0, 1) * K^(-1/4) on each operand
 c4     8192 x 8192 x 8192       U[-1, 1]
 c5     128 x 14336 x 4096       A ~ N(0, 1), B ~ N(0, 0.02^2)
+c6     81920 x 256 x 256        U[-1, 1] (the tall shape "cute(9)
+                                multistage_gemm" times in its section 11;
+                                the page does not state its values)
 =====  =======================  ===========================================
 """
 from __future__ import annotations
@@ -92,6 +95,7 @@ WORKLOADS = {
     "c3": dict(M=4096, N=4096, K=4096, kind="normal_k_quarter"),
     "c4": dict(M=8192, N=8192, K=8192, kind="uniform"),
     "c5": dict(M=128, N=14336, K=4096, kind="skinny"),
+    "c6": dict(M=81920, N=256, K=256, kind="uniform"),
 }
 WORKLOAD_NAMES = {
     "c1": "gemm_tn_f16 256x256x256 U[-1,1]",
@@ -99,11 +103,12 @@ WORKLOAD_NAMES = {
     "c3": "gemm_tn_f16 4096x4096x4096 N(0,1)*K^-1/4",
     "c4": "gemm_tn_f16 8192x8192x8192 U[-1,1]",
     "c5": "gemm_tn_f16 skinny M=128 N=14336 K=4096 A~N(0,1) B~N(0,0.02)",
+    "c6": "gemm_tn_f16 tall M=81920 N=256 K=256 U[-1,1]",
 }
 
 
 def seeds(tag: str) -> tuple[int, int, int]:
-    """(seed_A, seed_B, seed_samples) for a workload tag c1..c5."""
+    """(seed_A, seed_B, seed_samples) for a workload tag c1..c6."""
     c = int(tag[1:])
     return 1000 + c, 2000 + c, 3000 + c
 
@@ -123,7 +128,7 @@ def make_operands(kind: str, M: int, N: int, K: int, seed_a: int, seed_b: int):
 
 
 def workload(tag: str):
-    """(A_bits, B_bits, spec) for c1..c5."""
+    """(A_bits, B_bits, spec) for a workload tag c1..c6."""
     spec = WORKLOADS[tag]
     sa, sb, _ = seeds(tag)
     a, b = make_operands(spec["kind"], spec["M"], spec["N"], spec["K"], sa, sb)

@@ -82,7 +82,8 @@ def test_every_ring_depth_and_wrap(lib, gpu, path, bn):
     # K = BK * (kstage +- 1) around every depth: the ring wraps mid-tile and
     # the phase bits flip at different k-blocks; one CTA (pair) walks all
     # tiles so both TMEM accumulators are reused many times.
-    deepest = lib.query_config(256, 512, 4096, bn=bn, path=path)["kstage"]
+    fixed = dict(bn=bn, path=path, katoms=1, epi_warps=4)   # the ring depth alone varies
+    deepest = lib.query_config(256, 512, 4096, **fixed)["kstage"]
     a_full = synthetic.uniform_pm1(5, (512, 64 * (deepest + 2)))
     b_full = synthetic.uniform_pm1(6, (512, 64 * (deepest + 2)))
     for ks in range(2, deepest + 1):
@@ -90,8 +91,7 @@ def test_every_ring_depth_and_wrap(lib, gpu, path, bn):
             K = 64 * kb
             a = np.ascontiguousarray(a_full[:, :K])
             b = np.ascontiguousarray(b_full[:, :K])
-            got = _run(lib, a, b, gpu, bn=bn, kstage=ks, max_ctas=2 if path == PAIR else 1,
-                       path=path)
+            got = _run(lib, a, b, gpu, kstage=ks, max_ctas=2 if path == PAIR else 1, **fixed)
             _check(got, a, b)
 
 
@@ -100,14 +100,26 @@ def test_two_k_slices_per_stage(lib, gpu, path, bn):
     # katoms = 2: each ring stage holds two 64-wide K slices; K values put the
     # tail in the first or the second slice, or leave the second slice entirely
     # past K (its loads read zeros), and the ring wraps at every depth
-    deepest = lib.query_config(384, 520, 4096, bn=bn, path=path, katoms=2)["kstage"]
+    fixed = dict(bn=bn, path=path, katoms=2, epi_warps=8)
+    deepest = lib.query_config(384, 520, 4096, **fixed)["kstage"]
     for ks in range(2, deepest + 1):
         for K in (64, 120, 128, 136, 64 * 2 * ks + 64, 64 * 2 * (ks + 1) + 8):
             a = synthetic.uniform_pm1(K + ks, (384, K))
             b = synthetic.uniform_pm1(K + ks + 1, (520, K))
-            got = _run(lib, a, b, gpu, bn=bn, kstage=ks, katoms=2, path=path,
-                       max_ctas=2 if path == PAIR else 1)
+            got = _run(lib, a, b, gpu, kstage=ks, max_ctas=2 if path == PAIR else 1, **fixed)
             _check(got, a, b)
+
+
+@pytest.mark.parametrize("epi", [4, 8])
+@pytest.mark.parametrize("path,bn", [(SQUARE, 32), (SQUARE, 96), (SQUARE, 256), (PAIR, 64),
+                                     (PAIR, 160), (PAIR, 256)])
+def test_both_epilogue_widths(lib, gpu, epi, path, bn):
+    # 4 epilogue warps (one per TMEM lane quadrant) or 8 (two per quadrant,
+    # alternate 32-column chunks); N tails leave odd chunk counts per warp
+    for M, N, K in [(300, 8 * 41, 192), (129, 264, 64), (520, 1000, 320)]:
+        a = synthetic.uniform_pm1(M + epi, (M, K))
+        b = synthetic.uniform_pm1(N + epi, (N, K))
+        _check(_run(lib, a, b, gpu, path=path, bn=bn, epi_warps=epi, max_ctas=4), a, b)
 
 
 def test_two_k_slices_ternary_is_bit_exact(lib, gpu):
@@ -242,6 +254,12 @@ def test_workload_8192_sampled(lib, gpu):
 
 def test_workload_skinny(lib, gpu):
     st = _workload_check(lib, gpu, "c5")
+    assert st["exact_frac"] > 0.95
+
+
+def test_workload_tall(lib, gpu):
+    # the shape the multistage page times (section 11): 81920 x 256 x 256
+    st = _workload_check(lib, gpu, "c6")
     assert st["exact_frac"] > 0.95
 
 

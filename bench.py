@@ -208,6 +208,23 @@ def run_reference(args, tag):
     return 0
 
 
+def slowest_rank_ms(ms: float, world: int) -> float:
+    """The step time every rank agrees on: the maximum over ranks (gloo,
+    host tensors; the GEMM itself exchanges nothing between GPUs)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world: int, ms: float) -> float:
+    """Whole-job rate: the units every rank processed over the slowest rank's time."""
+    return units_per_rank * world / (ms * 1e-3)
+
+
 def workload_config(tag, spec, extra=None):
     c = {"workload": synthetic.WORKLOAD_NAMES[tag], "M": spec["M"], "N": spec["N"],
          "K": spec["K"], "layout": "TN: A MxK, B NxK row-major, D MxN row-major",
@@ -366,10 +383,7 @@ def run_gpu(args, tag):
                "mean_ms_write_only_flush": statistics.mean(iso_dirty),
                "note": "per-launch event pairs after an L2 flush; includes the isolated "
                        "launch latency (an empty kernel measures ~4.5 us this way)"}
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = slowest_rank_ms(ms, world)
     status, raw = binding.get_device_error(stream)
     if status != 0:
         raise SystemExit(f"device error in timed region: {raw:#x}")
@@ -392,10 +406,7 @@ def run_gpu(args, tag):
     e_end.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e_start.elapsed_time(e_end) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = slowest_rank_ms(e2e_ms, world)
 
     if rank != 0:
         return 0
@@ -430,7 +441,8 @@ def run_gpu(args, tag):
     roof["alg_bytes_per_launch"] = alg_bytes
     roof["flops_per_launch"] = flops
 
-    line = {"metric": METRIC, "value": tflops * world, "unit": UNIT, "n_gpus": world,
+    line = {"metric": METRIC, "value": job_throughput(flops, world, ms) / 1e12, "unit": UNIT,
+            "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
             "data": "synthetic (seeded splitmix64, fp16-rounded)",
@@ -453,7 +465,7 @@ def run_gpu(args, tag):
                           if launches_ms else {"mean": ms}),
             "launch_ms_isolated": iso,
             "roofline": roof,
-            "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+            "e2e": {"value": job_throughput(flops, world, e2e_ms) / 1e12, "unit": UNIT,
                     "h2d_bytes_per_step": 2 * (M * K + N * K), "d2h_bytes_per_step": 2 * M * N,
                     "ms_per_step": e2e_ms, "steps": e2e_steps},
             "gpu_launches": args.steps,

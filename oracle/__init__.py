@@ -14,6 +14,8 @@ with gcc into ``oracle/_build/`` and exposes it through ctypes:
   written from the IEEE 754 binary16 definition.
 * ``gemm_tn(a_bits, b_bits, threads)`` -- the full M x N product.
 * ``gemm_tn_sampled(a_bits, b_bits, rows, cols)`` -- selected elements.
+* ``gemm_scaled(a_bits, b_bits, c_bits, alpha, beta, b_kn)`` -- the scaled
+  form alpha * A op(B) + beta * C, with B N x K (TN) or K x N (NN).
 * ``minimum_stages(copy, compute)`` -- S_min = ceil(copy/compute) + 1
   ("第 6 课：Shared Memory 布局与异步流水", section 4).
 
@@ -56,6 +58,9 @@ def _bind(lib):
     lib.oracle_gemm_tn.restype = ctypes.c_int
     lib.oracle_gemm_tn_sampled.argtypes = [u16p, u16p, i64, i64, i64, i64p, i64p, i64, u16p]
     lib.oracle_gemm_tn_sampled.restype = ctypes.c_int
+    lib.oracle_gemm_scaled.argtypes = [u16p, u16p, u16p, u16p, i64, i64, i64, ctypes.c_float,
+                                       ctypes.c_float, ctypes.c_int, ctypes.c_int]
+    lib.oracle_gemm_scaled.restype = ctypes.c_int
     lib.oracle_minimum_stages.argtypes = [i64, i64]
     lib.oracle_minimum_stages.restype = ctypes.c_int64
     return lib
@@ -128,6 +133,36 @@ def gemm_tn(a_bits: np.ndarray, b_bits: np.ndarray, threads: int | None = None, 
                                 _ptr(d, ctypes.c_uint16), M, N, K, threads or default_threads())
     if rc != 0:
         raise ValueError("oracle_gemm_tn rejected its arguments")
+    return d
+
+
+def gemm_scaled(a_bits: np.ndarray, b_bits: np.ndarray, c_bits, alpha: float, beta: float,
+                b_kn: bool, threads: int | None = None, lib=None) -> np.ndarray:
+    """D = fp16(alpha * A op(B) + beta * C): B is K x N when b_kn, else N x K.
+    C (M x N fp16 bits) is not read when beta == 0 and may then be None."""
+    a, b = _u16(a_bits), _u16(b_bits)
+    M, K = a.shape
+    if b_kn:
+        if b.shape[0] != K:
+            raise ValueError("B must be K x N")
+        N = b.shape[1]
+    else:
+        if b.shape[1] != K:
+            raise ValueError("B must be N x K")
+        N = b.shape[0]
+    c = None
+    if c_bits is not None:
+        c = _u16(c_bits)
+        if c.shape != (M, N):
+            raise ValueError("C must be M x N")
+    d = np.zeros((M, N), dtype=np.uint16)
+    c_ptr = _ptr(c, ctypes.c_uint16) if c is not None else None
+    rc = (lib or _load()).oracle_gemm_scaled(_ptr(a, ctypes.c_uint16), _ptr(b, ctypes.c_uint16),
+                                            c_ptr, _ptr(d, ctypes.c_uint16), M, N, K,
+                                            float(alpha), float(beta), 1 if b_kn else 0,
+                                            threads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_gemm_scaled rejected its arguments")
     return d
 
 

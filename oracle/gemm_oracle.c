@@ -145,6 +145,80 @@ int oracle_gemm_tn(const uint16_t* A, const uint16_t* B, uint16_t* D,
     return 0;
 }
 
+/* ---- the scaled form: D = alpha * A op(B) + beta * C ---------------------
+ *
+ * "CUDA 算子笔记 2", section "General Matrix Multiplication（GEMM）", states the
+ * problem as C = alpha * A * B + beta * C with A M x K and B K x N row-major
+ * (the NN layout), fp16 matrices and fp32 alpha, beta (its "C is M x K" is a
+ * slip: C has the product's shape, M x N).  Written out:
+ *
+ *   D[i][j] = fp16_rne( alpha * sum_k A[i][k] * B(k, j) + beta * C[i][j] )
+ *
+ * with B(k, j) = B[k*N + j] when b_kn != 0 (B is K x N) and B[j*K + k] when
+ * b_kn == 0 (B is N x K, the TN case above).  alpha and beta are fp32 values,
+ * exact in double; the sum is the same double sum as oracle_gemm_tn; the
+ * combination alpha*s + beta*c is formed in double and rounded once to fp16.
+ * When beta == 0, C is not read (it may be NULL), as in BLAS.  D may be C. */
+typedef struct {
+    const uint16_t* A; const uint16_t* B; const uint16_t* C; uint16_t* D;
+    int64_t M, N, K, row_begin, row_end;
+    double alpha, beta;
+    int b_kn;
+} scaled_job;
+
+static void* run_scaled_rows(void* p)
+{
+    scaled_job* j = (scaled_job*)p;
+    for (int64_t i = j->row_begin; i < j->row_end; ++i) {
+        for (int64_t n = 0; n < j->N; ++n) {
+            double s = 0.0;
+            for (int64_t k = 0; k < j->K; ++k) {
+                const uint16_t b = j->b_kn ? j->B[k * j->N + n] : j->B[n * j->K + k];
+                s += oracle_half_to_double(j->A[i * j->K + k]) * oracle_half_to_double(b);
+            }
+            double v = j->alpha * s;
+            if (j->beta != 0.0) v += j->beta * oracle_half_to_double(j->C[i * j->N + n]);
+            j->D[i * j->N + n] = oracle_double_to_half(v);
+        }
+    }
+    return NULL;
+}
+
+int oracle_gemm_scaled(const uint16_t* A, const uint16_t* B, const uint16_t* C, uint16_t* D,
+                       int64_t M, int64_t N, int64_t K, float alpha, float beta, int b_kn,
+                       int threads)
+{
+    enum { MAX_THREADS = 256 };
+    if (M < 0 || N < 0 || K < 0) return -1;
+    if (M == 0 || N == 0) return 0;
+    if (!D || (K > 0 && (!A || !B)) || (beta != 0.0f && !C)) return -1;
+    if (threads < 1) threads = 1;
+    if (threads > MAX_THREADS) threads = MAX_THREADS;
+    if (threads > M) threads = (int)M;
+    /* D may be C: each element of C is read once, by the thread that then
+     * writes that element, before it writes it. */
+    pthread_t tid[MAX_THREADS];
+    int joined[MAX_THREADS];
+    scaled_job job[MAX_THREADS];
+    int64_t per = (M + threads - 1) / threads;
+    for (int t = 0; t < threads; ++t) {
+        int64_t b = t * per, e = (t + 1) * per;
+        if (b > M) b = M;
+        if (e > M) e = M;
+        job[t] = (scaled_job){A, B, C, D, M, N, K, b, e, (double)alpha, (double)beta, b_kn};
+        joined[t] = 0;
+    }
+    for (int t = 1; t < threads; ++t) {
+        if (job[t].row_begin >= job[t].row_end) continue;
+        if (pthread_create(&tid[t], NULL, run_scaled_rows, &job[t]) == 0) joined[t] = 1;
+        else run_scaled_rows(&job[t]);
+    }
+    run_scaled_rows(&job[0]);
+    for (int t = 1; t < threads; ++t)
+        if (joined[t]) pthread_join(tid[t], NULL);
+    return 0;
+}
+
 /* Selected elements only: out[s] = D[rows[s]][cols[s]].  Used where the full
  * product is too large for the CPU (the 8192^3 case). */
 int oracle_gemm_tn_sampled(const uint16_t* A, const uint16_t* B,

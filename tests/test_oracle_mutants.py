@@ -17,7 +17,10 @@ MUTANTS = {
     "transposed_result": ("dot_row_row(j->A + i * j->K, j->B + n * j->K, j->K)",
                           "dot_row_row(j->A + (n % j->M) * j->K, j->B + (i % j->N) * j->K, j->K)"),
     "b_row_from_i": ("j->B + n * j->K, j->K)", "j->B + (i % j->N) * j->K, j->K)"),
-    "float_accumulator": ("double s = 0.0;", "float s = 0.0f;"),
+    "float_accumulator": ("    double s = 0.0;\n    for (int64_t k = 0; k < K; ++k)",
+                          "    float s = 0.0f;\n    for (int64_t k = 0; k < K; ++k)"),
+    "scaled_float_accumulator": ("            double s = 0.0;\n            for (int64_t k = 0; k < j->K; ++k) {",
+                                 "            float s = 0.0f;\n            for (int64_t k = 0; k < j->K; ++k) {"),
     "round_via_float": ("j->D[i * j->N + n] = oracle_double_to_half(\n                dot_row_row(",
                         "j->D[i * j->N + n] = oracle_double_to_half((float)\n                dot_row_row("),
     "ties_to_odd": ("fmod(r, 2.0) != 0.0", "fmod(r, 2.0) == 0.0"),
@@ -27,6 +30,11 @@ MUTANTS = {
     "exponent_bias": ("expo - 25); /* 1.frac", "expo - 24); /* 1.frac"),
     "stages_floor": ("+ (copy_cycles % compute_cycles != 0);", ";"),
     "stages_no_plus_one": ("return in_flight + 1;", "return in_flight;"),
+    "scaled_drop_beta": ("if (j->beta != 0.0) v += j->beta * oracle_half_to_double(j->C[i * j->N + n]);", ""),
+    "scaled_alpha_skipped": ("double v = j->alpha * s;", "double v = s;"),
+    "scaled_nn_read_as_tn": ("j->b_kn ? j->B[k * j->N + n] : j->B[n * j->K + k]",
+                             "j->b_kn ? j->B[(n * j->K + k) % (j->K * j->N)] : j->B[n * j->K + k]"),
+    "scaled_beta_on_alpha": ("v += j->beta * oracle_half_to_double", "v += j->alpha * oracle_half_to_double"),
 }
 
 

@@ -161,6 +161,9 @@ def test_accumulation_is_wider_than_float(order):
     b = b.astype(np.float16).view(np.uint16)[None, :]
     assert int(oracle.gemm_tn(a, b)[0, 0]) == 0x3C01
     assert int(_exact_reference(a, b)[0, 0]) == 0x3C01
+    # the scaled form accumulates the same way (alpha = 1, beta = 0), in both layouts
+    assert int(oracle.gemm_scaled(a, b, None, 1.0, 0.0, False)[0, 0]) == 0x3C01
+    assert int(oracle.gemm_scaled(a, np.ascontiguousarray(b.T), None, 1.0, 0.0, True)[0, 0]) == 0x3C01
 
 
 def test_subnormal_and_overflow_results():
@@ -285,3 +288,100 @@ def test_generators_are_seeded_and_in_range():
     assert set(np.unique(t)) == {-1.0, 0.0, 1.0}
     n = synthetic.normal(3, 200_001)
     assert abs(n.mean()) < 0.01 and abs(n.std() - 1) < 0.01
+
+
+# --------------------------------------------------------------------------- scaled form
+# D = fp16(alpha * A op(B) + beta * C), "CUDA 算子笔记 2" (GEMM section):
+# C = alpha A B + beta C, fp16 matrices, fp32 alpha and beta, B K x N (NN).
+from fractions import Fraction  # noqa: E402
+
+
+def _fraction_to_half_bits(x: Fraction) -> int:
+    """Round an exact rational to binary16, nearest-even, by exact rational
+    arithmetic (no floating point on the way)."""
+    neg = x < 0
+    a = -x if neg else x
+    if a == 0:
+        return 0x8000 if neg else 0
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    elif Fraction(2) ** (e + 1) <= a:
+        e += 1
+    q = Fraction(2) ** (max(e, -14) - 10)           # binary16 spacing at a
+    n, rem = divmod(a, q)
+    half = q / 2
+    if rem > half or (rem == half and n % 2 == 1):
+        n += 1
+    mag = n * q
+    if mag > 65504:
+        bits = 0x7C00
+    else:
+        bits = int(np.float16(float(mag)).view(np.uint16))   # exactly representable
+    return bits | (0x8000 if neg else 0)
+
+
+def _exact_scaled(a_bits, b_bits, c_bits, alpha, beta, b_kn):
+    a = a_bits.view(np.float16).astype(np.float64)
+    b = b_bits.view(np.float16).astype(np.float64)
+    if not b_kn:
+        b = b.T
+    M, K = a.shape
+    N = b.shape[1]
+    al, be = Fraction(float(np.float32(alpha))), Fraction(float(np.float32(beta)))
+    c = c_bits.view(np.float16).astype(np.float64) if c_bits is not None else None
+    out = np.zeros((M, N), dtype=np.uint16)
+    for i in range(M):
+        for j in range(N):
+            s = sum(Fraction(a[i, k]) * Fraction(b[k, j]) for k in range(K))
+            v = al * s + (be * Fraction(c[i, j]) if be != 0 else 0)
+            out[i, j] = _fraction_to_half_bits(v)
+    return out
+
+
+@pytest.mark.parametrize("alpha,beta", [(1.0, 0.0), (0.5, -2.0), (-0.25, 1.0), (2.0, 0.75)])
+@pytest.mark.parametrize("b_kn", [False, True])
+def test_scaled_small_integers_exact(alpha, beta, b_kn):
+    rng = np.random.default_rng(17)
+    M, N, K = 7, 12, 9
+    ai = rng.integers(-3, 4, (M, K))
+    bi = rng.integers(-3, 4, (K, N))
+    ci = rng.integers(-50, 51, (M, N))
+    a = ai.astype(np.float16).view(np.uint16)
+    b = (bi if b_kn else bi.T).astype(np.float16).view(np.uint16)
+    c = ci.astype(np.float16).view(np.uint16)
+    want = (alpha * (ai @ bi) + beta * ci).astype(np.float16).view(np.uint16)  # exact dyadics
+    assert np.array_equal(oracle.gemm_scaled(a, b, c, alpha, beta, b_kn), want)
+
+
+@pytest.mark.parametrize("b_kn", [False, True])
+def test_scaled_random_against_exact_rational(b_kn):
+    rng = np.random.default_rng(23 + b_kn)
+    M, N, K = 5, 6, 40
+    a = rng.uniform(-1, 1, (M, K)).astype(np.float16).view(np.uint16)
+    b = rng.uniform(-1, 1, (K, N) if b_kn else (N, K)).astype(np.float16).view(np.uint16)
+    c = rng.uniform(-4, 4, (M, N)).astype(np.float16).view(np.uint16)
+    for alpha, beta in [(1.3, -0.7), (-0.01171875, 3.25), (0.1, 0.9)]:
+        got = oracle.gemm_scaled(a, b, c, alpha, beta, b_kn)
+        assert np.array_equal(got, _exact_scaled(a, b, c, alpha, beta, b_kn)), (alpha, beta)
+
+
+def test_scaled_special_cases():
+    rng = np.random.default_rng(29)
+    M, N, K = 9, 16, 24
+    a = rng.standard_normal((M, K)).astype(np.float16).view(np.uint16)
+    b_kn = rng.standard_normal((K, N)).astype(np.float16).view(np.uint16)
+    c = rng.standard_normal((M, N)).astype(np.float16).view(np.uint16)
+    # alpha = 0, beta = 1: D is C, bit for bit
+    assert np.array_equal(oracle.gemm_scaled(a, b_kn, c, 0.0, 1.0, True), c)
+    # beta = 0: C is never read -- NaN in C, or no C at all, changes nothing
+    c_nan = np.full((M, N), 0x7E00, np.uint16)
+    d0 = oracle.gemm_scaled(a, b_kn, c_nan, 1.5, 0.0, True)
+    assert np.array_equal(d0, oracle.gemm_scaled(a, b_kn, None, 1.5, 0.0, True))
+    assert not np.isnan(d0.view(np.float16)).any()
+    # NN on B equals TN on B's transpose, and alpha = 1, beta = 0 is the plain product
+    b_nk = np.ascontiguousarray(b_kn.T)
+    assert np.array_equal(oracle.gemm_scaled(a, b_kn, c, 0.8, -0.3, True),
+                          oracle.gemm_scaled(a, b_nk, c, 0.8, -0.3, False))
+    assert np.array_equal(oracle.gemm_scaled(a, b_nk, None, 1.0, 0.0, False),
+                          oracle.gemm_tn(a, b_nk))

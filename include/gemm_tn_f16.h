@@ -92,6 +92,35 @@ typedef struct {
 int gemm_tn_f16_ex(void* D, const void* A, const void* B, int64_t M, int64_t N, int64_t K,
                    const gemm_options_t* opt, void* stream);
 
+/* B operand layouts for gemm_f16_scaled. */
+enum {
+  GEMM_B_NK = 0,   /* B is N x K row-major (leading dimension K): D = alpha A B^T + beta C */
+  GEMM_B_KN = 1    /* B is K x N row-major (leading dimension N): D = alpha A B + beta C   */
+};
+
+/*
+ * gemm_f16_scaled: D = fp16_rn( alpha * A op(B) + beta * C ), fp32 accumulation
+ * and fp32 alpha, beta -- the problem "CUDA 算子笔记 2" states in its GEMM
+ * section (C = alpha A B + beta C with fp16 matrices and fp32 scalars; its
+ * B is K x N, i.e. GEMM_B_KN).
+ *
+ *   D  device, M*N fp16, row-major, leading dimension N.  Written only.
+ *   C  device, M*N fp16, row-major, leading dimension N.  Read only, and only
+ *      when beta != 0 (it may then be NULL).  C may be D itself (in place:
+ *      C = alpha A B + beta C); any other overlap of C and D is rejected.
+ *   A  device, M*K fp16, row-major.
+ *   B  device: N*K row-major for GEMM_B_NK, K*N row-major for GEMM_B_KN.
+ *
+ * Requirements and errors are those of gemm_tn_f16, plus: C 16-byte aligned
+ * when read; alpha and beta finite; b_layout one of GEMM_B_*.  With
+ * GEMM_B_KN the tile width is a multiple of 64 (128 on the pair path); an
+ * explicit opt->bn that is not is GEMM_ERR_INVALID_VALUE.  K == 0 writes
+ * D = beta * C (rounded to fp16).  opt may be NULL.  Asynchronous on stream.
+ */
+int gemm_f16_scaled(void* D, const void* C, const void* A, const void* B, int64_t M, int64_t N,
+                    int64_t K, float alpha, float beta, int b_layout, const gemm_options_t* opt,
+                    void* stream);
+
 /* Chosen configuration for a shape (host only, no GPU work; needs a current
  * device only to read its SM count -- with no device, 148 SMs are assumed). */
 typedef struct {

@@ -23,7 +23,10 @@ GEMM_ERR_CUDA = 6
 
 PATH_AUTO, PATH_SQUARE, PATH_SKINNY, PATH_PAIR = 0, 1, 2, 3
 
-EXPORTED = ("gemm_tn_f16", "gemm_tn_f16_ex", "gemm_query_config", "gemm_get_device_error",
+B_NK, B_KN = 0, 1
+
+EXPORTED = ("gemm_tn_f16", "gemm_tn_f16_ex", "gemm_f16_scaled", "gemm_query_config",
+            "gemm_get_device_error",
             "gemm_minimum_stages", "gemm_probe_latencies", "gemm_probe_latencies_static",
             "gemm_status_string")
 
@@ -61,6 +64,9 @@ def _load() -> ctypes.CDLL:
     lib.gemm_tn_f16.restype = i32
     lib.gemm_tn_f16_ex.argtypes = [vp, vp, vp, i64, i64, i64, ctypes.POINTER(GemmOptions), vp]
     lib.gemm_tn_f16_ex.restype = i32
+    lib.gemm_f16_scaled.argtypes = [vp, vp, vp, vp, i64, i64, i64, ctypes.c_float, ctypes.c_float,
+                                    i32, ctypes.POINTER(GemmOptions), vp]
+    lib.gemm_f16_scaled.restype = i32
     lib.gemm_query_config.argtypes = [i64, i64, i64, ctypes.POINTER(GemmOptions),
                                       ctypes.POINTER(GemmConfig)]
     lib.gemm_query_config.restype = i32
@@ -139,6 +145,50 @@ def gemm_tn_f16_ex(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = 
                                 ctypes.byref(o), _stream_handle(stream))
     if rc != GEMM_OK:
         raise GemmError(rc, "gemm_tn_f16_ex")
+    return out
+
+
+def gemm_f16_scaled(a: torch.Tensor, b: torch.Tensor, c: torch.Tensor | None = None,
+                    alpha: float = 1.0, beta: float = 0.0, b_layout: str = "kn",
+                    out: torch.Tensor | None = None, stream=None, **opts) -> torch.Tensor:
+    """out = alpha * A @ op(B) + beta * C via the C-ABI (fp32 accumulate, fp16 out).
+
+    b_layout "kn": B is K x N (out = alpha A B + beta C); "nk": B is N x K
+    (out = alpha A B^T + beta C).  C is read only when beta != 0; passing
+    out=c updates C in place."""
+    if b_layout not in ("kn", "nk"):
+        raise ValueError("b_layout must be 'kn' or 'nk'")
+    kn = b_layout == "kn"
+    if a.dtype != torch.float16 or b.dtype != torch.float16:
+        raise TypeError("A and B must be float16")
+    if a.dim() != 2 or b.dim() != 2 or not (a.is_cuda and b.is_cuda):
+        raise ValueError("A and B must be 2-D CUDA tensors")
+    if not (a.is_contiguous() and b.is_contiguous()):
+        raise ValueError("A and B must be contiguous (row-major)")
+    M, K = a.shape
+    if kn:
+        if b.shape[0] != K:
+            raise ValueError(f"B must be K x N, got {tuple(b.shape)}")
+        N = b.shape[1]
+    else:
+        if b.shape[1] != K:
+            raise ValueError(f"B must be N x K, got {tuple(b.shape)}")
+        N = b.shape[0]
+    if c is not None and (c.dtype != torch.float16 or tuple(c.shape) != (M, N)
+                          or not c.is_contiguous() or c.device != a.device):
+        raise ValueError("C must be a contiguous float16 M x N tensor on A's device")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=a.device)
+    elif out.dtype != torch.float16 or tuple(out.shape) != (M, N) or not out.is_contiguous() \
+            or out.device != a.device:
+        raise ValueError("out must be a contiguous float16 M x N tensor on A's device")
+    o = _options(**opts)
+    with torch.cuda.device(a.device):
+        rc = LIB.gemm_f16_scaled(out.data_ptr(), c.data_ptr() if c is not None else None,
+                                 a.data_ptr(), b.data_ptr(), M, N, K, float(alpha), float(beta),
+                                 B_KN if kn else B_NK, ctypes.byref(o), _stream_handle(stream))
+    if rc != GEMM_OK:
+        raise GemmError(rc, "gemm_f16_scaled")
     return out
 
 

@@ -150,10 +150,15 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
                 tma_load_2d_hint(ad, &tmA, full_bar(stage), x, mb * kBM, pol_a);
               else
                 tma_load_2d(ad, &tmA, full_bar(stage), x, mb * kBM);
-              if (p.l2_hints & 1u)
+              if (p.b_kn) {  // B is K x N: one 64-column box per chunk of the tile
+                for (int ch = 0; ch < p.bn / 64; ++ch)
+                  tma_load_2d(bd + ch * kMnChunkBytes, &tmB, full_bar(stage), nb * p.bn + 64 * ch,
+                              x);
+              } else if (p.l2_hints & 1u) {
                 tma_load_2d_hint(bd, &tmB, full_bar(stage), x, nb * p.bn, pol_b);
-              else
+              } else {
                 tma_load_2d(bd, &tmB, full_bar(stage), x, nb * p.bn);
+              }
             }
           }
           ++issued;
@@ -173,6 +178,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
+      const uint64_t b_kstep = p.b_kn ? 128u : 2u;  // descriptor address units per K = 16
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -194,12 +200,15 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
           const uint32_t b_src = a_src + p.katoms * kABytes;
           for (int at = 0; at < p.katoms; ++at) {
             const uint64_t a_desc = sw128_kmajor_desc(a_src + at * kABytes);
-            const uint64_t b_desc = sw128_kmajor_desc(b_src + at * p.b_atom_bytes);
+            const uint64_t b_desc =
+                p.b_kn ? sw128_mnmajor_desc(b_src + at * p.b_atom_bytes, kMnChunkBytes)
+                       : sw128_kmajor_desc(b_src + at * p.b_atom_bytes);
 #pragma unroll
             for (int k = 0; k < kBK / kUmmaK; ++k) {
-              // +32 bytes along K inside the 128-byte swizzle row = +2 in the
-              // descriptor's address field (16-byte units)
-              umma_f16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, p.idesc, (i | at | k) != 0);
+              // K-major: +32 bytes along K inside the 128-byte swizzle row = +2
+              // in the descriptor's address field (16-byte units); MN-major:
+              // +16 rows of 128 bytes = +128
+              umma_f16(d_tmem, a_desc + 2u * k, b_desc + b_kstep * k, p.idesc, (i | at | k) != 0);
             }
           }
           umma_commit(empty_bar(stage));  // frees the stage once these MMAs have read it
@@ -254,6 +263,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(tempty_bar(acc));
         }
+        if (p.scaled) apply_alpha_beta(r, p, m0 + lane, n0 + c * kEpiCols);
         const uint32_t buf = my_bufs + (chunk_seq % kEpiBufs) * kEpiChunkBytes;
         if (chunk_seq >= static_cast<uint32_t>(kEpiBufs)) {
           if (lane == 0) bulk_wait_group_read<kEpiBufs - 1>();  // buffer's last store has read it

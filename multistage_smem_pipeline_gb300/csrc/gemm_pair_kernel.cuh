@@ -126,10 +126,14 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
                 tma_load_2d_pair_hint(ad, &tmA, leader_full, x, a_row, pol_a);
               else
                 tma_load_2d_pair(ad, &tmA, leader_full, x, a_row);
-              if (p.l2_hints & 1u)
+              if (p.b_kn) {  // B is K x N: one 64-column box per chunk of this CTA's half
+                for (int ch = 0; ch < half_bn / 64; ++ch)
+                  tma_load_2d_pair(bd + ch * kMnChunkBytes, &tmB, leader_full, b_row + 64 * ch, x);
+              } else if (p.l2_hints & 1u) {
                 tma_load_2d_pair_hint(bd, &tmB, leader_full, x, b_row, pol_b);
-              else
+              } else {
                 tma_load_2d_pair(bd, &tmB, leader_full, x, b_row);
+              }
             }
           }
           ++issued;
@@ -149,6 +153,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (even CTA)
     if (lane == 0 && rank == 0) {
+      const uint64_t b_kstep = p.b_kn ? 128u : 2u;  // descriptor address units per K = 16
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -170,10 +175,13 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
           const uint32_t b_src = a_src + p.katoms * kABytes;
           for (int at = 0; at < p.katoms; ++at) {
             const uint64_t a_desc = sw128_kmajor_desc(a_src + at * kABytes);
-            const uint64_t b_desc = sw128_kmajor_desc(b_src + at * p.b_atom_bytes);
+            const uint64_t b_desc =
+                p.b_kn ? sw128_mnmajor_desc(b_src + at * p.b_atom_bytes, kMnChunkBytes)
+                       : sw128_kmajor_desc(b_src + at * p.b_atom_bytes);
 #pragma unroll
             for (int k = 0; k < kBK / kUmmaK; ++k)
-              umma_f16_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, p.idesc, (i | at | k) != 0);
+              umma_f16_pair(d_tmem, a_desc + 2u * k, b_desc + b_kstep * k, p.idesc,
+                            (i | at | k) != 0);
           }
           umma_commit_pair_mc(empty_bar(stage), 0x3);
           if (++stage == S) {
@@ -227,6 +235,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(leader_tempty);
         }
+        if (p.scaled) apply_alpha_beta(r, p, m0 + lane, n0 + c * kEpiCols);
         const uint32_t buf = my_bufs + (chunk_seq % kEpiBufs) * kEpiChunkBytes;
         if (chunk_seq >= static_cast<uint32_t>(kEpiBufs)) {
           if (lane == 0) bulk_wait_group_read<kEpiBufs - 1>();

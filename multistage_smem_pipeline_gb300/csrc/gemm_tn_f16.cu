@@ -1,10 +1,12 @@
 // Host side of the C-ABI: argument checks, configuration choice, TMA
 // descriptor encoding and the launch of the persistent kernel.
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
 #include <climits>
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -123,7 +125,7 @@ struct Plan {
 };
 
 int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sms, int max_pairs,
-              Plan* out) {
+              Plan* out, int b_kn = 0) {
   gemm_options_t o;
   std::memset(&o, 0, sizeof(o));
   if (opt) o = *opt;
@@ -155,6 +157,8 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
     }
     for (int cand = 256; cand >= 32; cand -= 32) {
       if (o.bn && cand != o.bn) continue;
+      // a K x N B is loaded in 64-column boxes: each CTA's share of BN must be whole boxes
+      if (b_kn && cand % (kind == GEMM_PATH_PAIR ? 128 : 64) != 0) continue;
       const int bm = (kind == GEMM_PATH_PAIR) ? 2 * kBM : kBM;
       const int64_t tiles = ((M + bm - 1) / bm) * ((N + cand - 1) / cand);
       const int64_t slots = (kind == GEMM_PATH_PAIR) ? max_pairs : sms;
@@ -230,7 +234,8 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   p.num_k_blocks = static_cast<int32_t>(num_k);
   p.num_tiles = static_cast<int32_t>(tiles);
   p.group_m = group_m;
-  p.idesc = make_idesc(bm, bn);
+  p.idesc = make_idesc(bm, bn) | (b_kn ? (1u << 16) : 0u);  // bit 16: B is MN-major
+  p.b_kn = b_kn;
   p.tmem_cols = pow2_at_least(2u * bn);
   p.stage_bytes = stage_bytes;
   p.b_atom_bytes = b_atom_bytes_for(path, bn);
@@ -320,14 +325,45 @@ int check_args(const void* D, const void* A, const void* B, int64_t M, int64_t N
   return GEMM_OK;
 }
 
+// The scaled form D = alpha * A op(B) + beta * C (nullptr: D = A B^T).
+struct Scaled {
+  const void* C;
+  float alpha, beta;
+  int b_kn;
+};
+
+// D = beta * C elementwise: the scaled form with an empty k range.
+__global__ void scale_c_kernel(uint16_t* D, const uint16_t* C, float beta, int64_t n) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float c = __half2float(__ushort_as_half(C[i]));
+    D[i] = __half_as_ushort(__float2half_rn(beta * c));
+  }
+}
+
+int check_scaled(const void* D, const Scaled& sc, int64_t M, int64_t N) {
+  if (sc.b_kn != 0 && sc.b_kn != 1) return GEMM_ERR_INVALID_VALUE;
+  if (!std::isfinite(sc.alpha) || !std::isfinite(sc.beta)) return GEMM_ERR_INVALID_VALUE;
+  if (sc.beta == 0.0f || M == 0 || N == 0) return GEMM_OK;  // C is not read
+  if (!sc.C) return GEMM_ERR_INVALID_VALUE;
+  if (reinterpret_cast<uintptr_t>(sc.C) & 15) return GEMM_ERR_MISALIGNED;
+  const uint64_t bytes = static_cast<uint64_t>(M) * N * 2;
+  // C may be D exactly (in place: each element is read before the same CTA
+  // writes it); any other overlap would read partly written values.
+  if (sc.C != D && overlaps(sc.C, bytes, D, bytes)) return GEMM_ERR_INVALID_VALUE;
+  return GEMM_OK;
+}
+
 int run(void* D, const void* A, const void* B, int64_t M, int64_t N, int64_t K,
-        const gemm_options_t* opt, cudaStream_t stream) {
+        const gemm_options_t* opt, cudaStream_t stream, const Scaled* sc = nullptr) {
   int rc = check_args(D, A, B, M, N, K);
   if (rc != GEMM_OK) return rc;
+  const int b_kn = sc ? sc->b_kn : 0;
+  if (sc && (rc = check_scaled(D, *sc, M, N)) != GEMM_OK) return rc;
   if (opt) {  // validate options even when there is nothing to compute
     Plan tmp;
     rc = make_plan(std::max<int64_t>(M, 1), std::max<int64_t>(N, 8), std::max<int64_t>(K, 8), opt,
-                   148, 74, &tmp);
+                   148, 74, &tmp, b_kn);
     if (rc != GEMM_OK) return rc;
   }
   if (M == 0 || N == 0) return GEMM_OK;
@@ -335,7 +371,14 @@ int run(void* D, const void* A, const void* B, int64_t M, int64_t N, int64_t K,
   DeviceState* st = nullptr;
   rc = current_device(&dev, &st);
   if (rc != GEMM_OK) return rc;
-  if (K == 0) {
+  if (K == 0) {  // the empty sum: D = 0, or D = beta * C in the scaled form
+    if (sc && sc->beta != 0.0f) {
+      const int64_t n = M * N;
+      const int blocks = static_cast<int>(std::min<int64_t>((n + 255) / 256, 8 * st->sm_count));
+      scale_c_kernel<<<blocks, 256, 0, stream>>>(static_cast<uint16_t*>(D),
+                                                 static_cast<const uint16_t*>(sc->C), sc->beta, n);
+      return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
+    }
     if (cudaMemsetAsync(D, 0, static_cast<size_t>(M) * N * 2, stream) != cudaSuccess) {
       cudaGetLastError();
       return GEMM_ERR_CUDA;
@@ -344,15 +387,23 @@ int run(void* D, const void* A, const void* B, int64_t M, int64_t N, int64_t K,
   }
   if ((rc = prepare_device(st)) != GEMM_OK) return rc;
   Plan pl;
-  rc = make_plan(M, N, K, opt, st->sm_count, st->max_pairs, &pl);
+  rc = make_plan(M, N, K, opt, st->sm_count, st->max_pairs, &pl, b_kn);
   if (rc != GEMM_OK) return rc;
   if ((rc = get_encoder()) != GEMM_OK) return rc;
+  if (sc && !(sc->alpha == 1.0f && sc->beta == 0.0f)) {
+    pl.p.scaled = 1;
+    pl.p.alpha = sc->alpha;
+    pl.p.beta = sc->beta;
+    pl.p.C = static_cast<const uint16_t*>(sc->C);
+  }
 
   const bool pair = pl.cfg.path == GEMM_PATH_PAIR;
   const uint32_t b_box_rows = pair ? pl.cfg.bn / 2 : pl.cfg.bn;
   CUtensorMap tmA, tmB, tmD;
+  const int b_rc = b_kn ? encode_2d(&tmB, B, N, K, 64, kBK, CU_TENSOR_MAP_SWIZZLE_128B)
+                        : encode_2d(&tmB, B, K, N, kBK, b_box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
   if (encode_2d(&tmA, A, K, M, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B) != GEMM_OK ||
-      encode_2d(&tmB, B, K, N, kBK, b_box_rows, CU_TENSOR_MAP_SWIZZLE_128B) != GEMM_OK ||
+      b_rc != GEMM_OK ||
       encode_2d(&tmD, D, N, M, kEpiCols, 32, CU_TENSOR_MAP_SWIZZLE_64B) != GEMM_OK)
     return GEMM_ERR_INVALID_VALUE;
 
@@ -398,6 +449,13 @@ using namespace gb300;
 extern "C" int gemm_tn_f16(void* D, const void* A, const void* B, int64_t M, int64_t N, int64_t K,
                            void* stream) {
   return run(D, A, B, M, N, K, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int gemm_f16_scaled(void* D, const void* C, const void* A, const void* B, int64_t M,
+                               int64_t N, int64_t K, float alpha, float beta, int b_layout,
+                               const gemm_options_t* opt, void* stream) {
+  const Scaled sc{C, alpha, beta, b_layout};
+  return run(D, A, B, M, N, K, opt, static_cast<cudaStream_t>(stream), &sc);
 }
 
 extern "C" int gemm_tn_f16_ex(void* D, const void* A, const void* B, int64_t M, int64_t N,

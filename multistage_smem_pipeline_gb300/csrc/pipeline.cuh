@@ -42,7 +42,14 @@ struct GemmParams {
   int32_t inject;
   int32_t k_rotate;      // 1: each tile starts its k loop at a tile-dependent k-block
   int32_t epi_warps;     // epilogue warps (4 or 8); must match the launched kernel
+  int32_t b_kn;          // 1: B is K x N row-major (N contiguous): an MN-major operand
+  int32_t scaled;        // 1: D = alpha * acc + beta * C instead of D = acc
+  float alpha, beta;
+  const uint16_t* C;     // M x N fp16, row stride N; read only when scaled and beta != 0
 };
+
+// MN-major B: one 64-element N chunk per TMA box; chunks 8 KiB apart.
+constexpr uint32_t kMnChunkBytes = 64 * 64 * 2;
 
 // First k-block of tile t.  With rotation the tiles in flight start at
 // evenly spread k offsets, so when every tile reads the same rows of A (one
@@ -101,6 +108,32 @@ __device__ __forceinline__ void tile_coords(int t, const GemmParams& p, int& mb,
 __device__ __forceinline__ uint32_t pack_half2(uint32_t lo_bits, uint32_t hi_bits) {
   const __half2 h = __floats2half2_rn(__uint_as_float(lo_bits), __uint_as_float(hi_bits));
   return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// r (fp32 bits of one row's 32 accumulator columns) <- alpha * r + beta * C
+// for row `row`, columns [col, col + 32) of C.  Groups of 8 columns past N,
+// and rows past M, are not read (N is a multiple of 8).
+__device__ __forceinline__ void apply_alpha_beta(uint32_t (&r)[32], const GemmParams& p, int row,
+                                                 int col) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(p.alpha * __uint_as_float(r[i]));
+  if (p.beta == 0.0f || row >= p.M) return;
+  const uint16_t* c_row = p.C + static_cast<size_t>(row) * p.N + col;
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    if (col + 8 * g < p.N) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(c_row + 8 * g));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const __half2 h = *reinterpret_cast<const __half2*>(&w[q]);
+        const float2 f = __half22float2(h);
+        r[8 * g + 2 * q] = __float_as_uint(fmaf(p.beta, f.x, __uint_as_float(r[8 * g + 2 * q])));
+        r[8 * g + 2 * q + 1] =
+            __float_as_uint(fmaf(p.beta, f.y, __uint_as_float(r[8 * g + 2 * q + 1])));
+      }
+    }
+  }
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,

@@ -206,6 +206,22 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
   return d;
 }
 
+// Shared-memory matrix descriptor for an MN-major operand tile written by
+// TMA with 128-byte swizzling: each 64-element MN chunk is a stack of 8-row
+// (8 K values) atoms of 1024 B; `lbo_bytes` separates consecutive 64-element
+// MN chunks (leading byte offset, bits 16-29) and 1024 B separates 8-row K
+// groups (stride byte offset, bits 32-45).  Same version and layout fields as
+// the K-major form.  One K = 16 step of an MMA covers two K groups: +2048 B.
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t smem_addr, uint32_t lbo_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
 }  // namespace gb300
 
 // ---------------------------------------------------------------- CTA pairs (cluster of 2)

@@ -31,7 +31,8 @@ def _declared_functions():
 
 def test_header_declares_the_boundary():
     names = _declared_functions()
-    for want in ("gemm_tn_f16", "gemm_tn_f16_ex", "gemm_get_device_error", "gemm_minimum_stages",
+    for want in ("gemm_tn_f16", "gemm_tn_f16_ex", "gemm_f16_scaled", "gemm_get_device_error",
+                 "gemm_minimum_stages",
                  "gemm_query_config", "gemm_probe_latencies", "gemm_status_string"):
         assert want in names
 
@@ -142,6 +143,28 @@ def test_query_config_plans(binding):
     for shape in [(8192, 8192, 8192), (128, 14336, 4096), (256, 256, 256)]:
         cc = binding.query_config(*shape)
         assert cc["katoms"] == 1 or cc["kstage"] >= 3
+
+
+def _scaled(binding, D, C, A, B, M, N, K, alpha=1.0, beta=0.0, layout=1, opts=None):
+    o = binding._options(**(opts or {}))
+    return binding.LIB.gemm_f16_scaled(D, C, A, B, M, N, K, alpha, beta, layout,
+                                       ctypes.byref(o), None)
+
+
+def test_scaled_entry_rejects_bad_arguments(binding):
+    E = binding.GEMM_ERR_INVALID_VALUE
+    assert _scaled(binding, P0, P1, P1 + 4096, P2, 16, 16, 16, layout=2) == E
+    assert _scaled(binding, P0, P1, P1 + 4096, P2, 16, 16, 16, alpha=float("nan")) == E
+    assert _scaled(binding, P0, P1, P1 + 4096, P2, 16, 16, 16, beta=float("inf")) == E
+    # beta != 0 needs C; C partially overlapping D is refused; C == D is allowed (in place)
+    assert _scaled(binding, P0, 0, P1, P2, 16, 16, 16, beta=0.5) == E
+    assert _scaled(binding, P0, P0 + 256, P1, P2, 16, 16, 16, beta=0.5) == E
+    assert _scaled(binding, P0, P0 + 8, P1, P2, 16, 16, 16, beta=0.5) == \
+        binding.GEMM_ERR_MISALIGNED
+    # a K x N B is loaded in 64-column boxes: the tile width must be whole boxes
+    assert _scaled(binding, P0, 0, P1, P2, 256, 256, 256, opts=dict(bn=96, path=1)) == E
+    assert _scaled(binding, P0, 0, P1, P2, 256, 256, 256, opts=dict(bn=64, path=3)) == E
+    assert _scaled(binding, 0, 0, 0, 0, 0, 16, 16, beta=0.5) == binding.GEMM_OK
 
 
 def test_status_strings(binding):

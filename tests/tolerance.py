@@ -54,3 +54,24 @@ def probes_agree(a: tuple, b: tuple) -> bool:
     (c1, m1), (c2, m2) = a, b
     return (abs(c1 - c2) <= PROBE_REL_TOL["copy"] * max(c1, c2)
             and abs(m1 - m2) <= PROBE_REL_TOL["compute"] * max(m1, m2))
+
+
+def compare_scaled(got_bits, ref_bits, K, a_bits, b_bits, c_bits, alpha, beta) -> dict:
+    """compare() for D = alpha * A op(B) + beta * C: the product term's bound
+    scales with |alpha|, and beta * C adds fp32 rounding of its own
+    (2^-20 |beta| max|C| is several fp32 ulps)."""
+    g = got_bits.view(np.float16).astype(np.float64)
+    r = ref_bits.view(np.float16).astype(np.float64)
+    amax = float(np.abs(a_bits.view(np.float16).astype(np.float64)).max()) if a_bits.size else 0.0
+    bmax = float(np.abs(b_bits.view(np.float16).astype(np.float64)).max()) if b_bits.size else 0.0
+    cmax = 0.0
+    if c_bits is not None and c_bits.size and beta != 0:
+        cmax = float(np.abs(c_bits.view(np.float16).astype(np.float64)).max())
+    tol = (2e-3 * np.sqrt(max(K, 1)) * abs(alpha) * amax * bmax + 2.0 ** -20 * abs(beta) * cmax
+           + fp16_ulp(r))
+    err = np.abs(g - r)
+    err = np.where(np.isnan(g) & np.isnan(r), 0.0, err)
+    err = np.where(np.isnan(err), np.inf, err)
+    return {"bad": int(np.count_nonzero(err > tol)), "max_err": float(err.max()) if err.size else 0.0,
+            "exact_frac": float(np.mean(got_bits == ref_bits)) if got_bits.size else 1.0,
+            "n": int(got_bits.size)}

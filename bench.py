@@ -257,34 +257,50 @@ def run_gpu(args, tag):
     b_host = torch.from_numpy(b_bits.view(np.float16)).pin_memory()
     a = a_host.to(dev)
     b = b_host.to(dev)
+    # the scaled form D = alpha A op(B) + beta C also reads C (M x N) each step
+    scaled = "alpha" in spec
+    b_kn = bool(spec.get("b_kn"))
+    if scaled:
+        c_host = torch.from_numpy(synthetic.workload_c(tag).view(np.float16)).pin_memory()
+        if spec["beta"] != 0:
+            alg_bytes += 2.0 * M * N
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     stream = torch.cuda.current_stream(dev)
     opts = {"path": ["auto", "square", "skinny", "pair"].index(args.path), "bn": args.bn,
             "kstage": args.kstage, "katoms": args.katoms, "group_m": args.group_m,
             "epi_warps": args.epi_warps}
     forced = any(opts.values())
-    cfg = binding.query_config(M, N, K, **opts)
+    cfg = binding.query_config(M, N, K, b_layout=1 if spec.get("b_kn") else 0, **opts)
 
     # Operand copies for the timed launches: launch i uses copy i % R, and the R
     # copies together span at least 3 x L2, so every launch reads operands that
     # the launches in between have evicted from L2 (inputs larger than L2).
     per_copy = int(alg_bytes)
     R = max(2, -(-3 * l2 // per_copy)) if args.timing == "rotate" else 1
+    b_shape = (K, N) if b_kn else (N, K)
     a_all = torch.empty((R, M, K), dtype=torch.float16, device=dev)
-    b_all = torch.empty((R, N, K), dtype=torch.float16, device=dev)
+    b_all = torch.empty((R,) + b_shape, dtype=torch.float16, device=dev)
     d_all = torch.empty((R, M, N), dtype=torch.float16, device=dev)
     a_all.copy_(a.unsqueeze(0).expand(R, M, K))
-    b_all.copy_(b.unsqueeze(0).expand(R, N, K))
+    b_all.copy_(b.unsqueeze(0).expand((R,) + b_shape))
+    c_all = None
+    if scaled:
+        c_all = torch.empty((R, M, N), dtype=torch.float16, device=dev)
+        c_all.copy_(c_host.to(dev).unsqueeze(0).expand(R, M, N))
     del a, b
 
-    def gemm(a_, b_, d_):
+    def gemm(a_, b_, d_, c_=None, stream_=None):
+        st = stream_ if stream_ is not None else stream
+        if scaled:
+            return binding.gemm_f16_scaled(a_, b_, c_, spec["alpha"], spec["beta"],
+                                           "kn" if b_kn else "nk", out=d_, stream=st, **opts)
         if forced:
-            return binding.gemm_tn_f16_ex(a_, b_, out=d_, stream=stream, **opts)
-        return binding.gemm_tn_f16(a_, b_, out=d_, stream=stream)
+            return binding.gemm_tn_f16_ex(a_, b_, out=d_, stream=st, **opts)
+        return binding.gemm_tn_f16(a_, b_, out=d_, stream=st)
 
     def launch(i):
         r = i % R
-        gemm(a_all[r], b_all[r], d_all[r])
+        gemm(a_all[r], b_all[r], d_all[r], c_all[r] if c_all is not None else None)
 
     for i in range(args.warmup):
         launch(i)
@@ -307,10 +323,8 @@ def run_gpu(args, tag):
                 cap = torch.cuda.current_stream(dev)
                 for i in range(n):
                     r = i % R
-                    if forced:
-                        binding.gemm_tn_f16_ex(a_all[r], b_all[r], out=d_all[r], stream=cap, **opts)
-                    else:
-                        binding.gemm_tn_f16(a_all[r], b_all[r], out=d_all[r], stream=cap)
+                    gemm(a_all[r], b_all[r], d_all[r], c_all[r] if c_all is not None else None,
+                         stream_=cap)
             return g
 
         graphs = (capture(R), capture(args.steps % R) if args.steps % R else None)
@@ -336,7 +350,7 @@ def run_gpu(args, tag):
             if sleep_cycles:
                 torch.cuda._sleep(sleep_cycles)
             st[i].record(stream)
-            gemm(a_all[0], b_all[0], d_all[0])
+            gemm(a_all[0], b_all[0], d_all[0], c_all[0] if c_all is not None else None)
             en[i].record(stream)
         torch.cuda.synchronize(dev)
         return [x.elapsed_time(y) for x, y in zip(st, en)]
@@ -401,7 +415,8 @@ def run_gpu(args, tag):
     for _ in range(e2e_steps):
         a_e = a_host.to(dev, non_blocking=True)
         b_e = b_host.to(dev, non_blocking=True)
-        gemm(a_e, b_e, d)
+        c_e = c_host.to(dev, non_blocking=True) if scaled else None
+        gemm(a_e, b_e, d, c_e)
         d_host.copy_(d, non_blocking=True)
     e_end.record(stream)
     torch.cuda.synchronize(dev)
@@ -466,7 +481,8 @@ def run_gpu(args, tag):
             "launch_ms_isolated": iso,
             "roofline": roof,
             "e2e": {"value": job_throughput(flops, world, e2e_ms) / 1e12, "unit": UNIT,
-                    "h2d_bytes_per_step": 2 * (M * K + N * K), "d2h_bytes_per_step": 2 * M * N,
+                    "h2d_bytes_per_step": 2 * (M * K + N * K + (M * N if scaled else 0)),
+                    "d2h_bytes_per_step": 2 * M * N,
                     "ms_per_step": e2e_ms, "steps": e2e_steps},
             "gpu_launches": args.steps,
             "clocks": clk,

@@ -84,6 +84,8 @@ typedef struct {
                           stage of 2 halves the per-byte barrier and commit work) */
   int epi_warps;       /* epilogue warps per CTA: 0 = choose, 4 or 8 (8 doubles the
                           TMEM -> global drain rate, for short k loops) */
+  int b_layout;        /* gemm_query_config only: plan for this B layout (GEMM_B_*);
+                          gemm_f16_scaled takes the layout as an argument */
 } gemm_options_t;
 
 /* gemm_tn_f16 with an explicit configuration (sweeps, tests).  Same

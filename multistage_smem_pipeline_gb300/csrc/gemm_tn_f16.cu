@@ -475,8 +475,10 @@ extern "C" int gemm_query_config(int64_t M, int64_t N, int64_t K, const gemm_opt
   } else {
     cudaGetLastError();
   }
+  const int b_kn = opt ? opt->b_layout : 0;
+  if (b_kn != 0 && b_kn != 1) return GEMM_ERR_INVALID_VALUE;
   Plan pl;
-  const int rc = make_plan(M, N, K, opt, sms, pairs, &pl);
+  const int rc = make_plan(M, N, K, opt, sms, pairs, &pl, b_kn);
   if (rc == GEMM_OK) *out = pl.cfg;
   return rc;
 }

@@ -23,6 +23,9 @@ c5     128 x 14336 x 4096       A ~ N(0, 1), B ~ N(0, 0.02^2)
 c6     81920 x 256 x 256        U[-1, 1] (the tall shape "cute(9)
                                 multistage_gemm" times in its section 11;
                                 the page does not state its values)
+c7     8192 x 8192 x 8192       U[-1, 1]; the scaled NN form of "CUDA 算子笔记
+                                2" (GEMM section): D = 1.5 A B - 0.5 C with
+                                B K x N and C U[-1, 1]
 =====  =======================  ===========================================
 """
 from __future__ import annotations
@@ -96,6 +99,7 @@ WORKLOADS = {
     "c4": dict(M=8192, N=8192, K=8192, kind="uniform"),
     "c5": dict(M=128, N=14336, K=4096, kind="skinny"),
     "c6": dict(M=81920, N=256, K=256, kind="uniform"),
+    "c7": dict(M=8192, N=8192, K=8192, kind="uniform", b_kn=True, alpha=1.5, beta=-0.5),
 }
 WORKLOAD_NAMES = {
     "c1": "gemm_tn_f16 256x256x256 U[-1,1]",
@@ -104,11 +108,12 @@ WORKLOAD_NAMES = {
     "c4": "gemm_tn_f16 8192x8192x8192 U[-1,1]",
     "c5": "gemm_tn_f16 skinny M=128 N=14336 K=4096 A~N(0,1) B~N(0,0.02)",
     "c6": "gemm_tn_f16 tall M=81920 N=256 K=256 U[-1,1]",
+    "c7": "gemm_f16_scaled NN 8192x8192x8192 D=1.5*A*B-0.5*C U[-1,1]",
 }
 
 
 def seeds(tag: str) -> tuple[int, int, int]:
-    """(seed_A, seed_B, seed_samples) for a workload tag c1..c6."""
+    """(seed_A, seed_B, seed_samples) for a workload tag c1..c7."""
     c = int(tag[1:])
     return 1000 + c, 2000 + c, 3000 + c
 
@@ -128,11 +133,22 @@ def make_operands(kind: str, M: int, N: int, K: int, seed_a: int, seed_b: int):
 
 
 def workload(tag: str):
-    """(A_bits, B_bits, spec) for a workload tag c1..c6."""
+    """(A_bits, B_bits, spec) for a workload tag c1..c7.  B is N x K, or K x N
+    where spec["b_kn"] is set."""
     spec = WORKLOADS[tag]
     sa, sb, _ = seeds(tag)
+    if spec.get("b_kn"):
+        if spec["kind"] != "uniform":
+            raise ValueError("K x N operands are generated for the uniform distribution only")
+        return uniform_pm1(sa, (spec["M"], spec["K"])), uniform_pm1(sb, (spec["K"], spec["N"])), spec
     a, b = make_operands(spec["kind"], spec["M"], spec["N"], spec["K"], sa, sb)
     return a, b, spec
+
+
+def workload_c(tag: str):
+    """C (M x N fp16 bits) of a scaled workload (seed 4000 + c)."""
+    spec = WORKLOADS[tag]
+    return uniform_pm1(4000 + int(tag[1:]), (spec["M"], spec["N"]))
 
 
 def sample_coords(seed: int, M: int, N: int, count: int = 4096, bm: int = 128, bn: int = 256):

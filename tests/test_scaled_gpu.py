@@ -124,3 +124,20 @@ def test_scaled_skinny_and_tall(lib, gpu):
             a, b, c = _operands(M, N, K, kn, M + K)
             got = _run(lib, gpu, a, b, c, 1.0, 1.0, kn)
             _check(got, a, b, c, 1.0, 1.0, kn)
+
+
+def test_workload_nn_scaled_8192_seeded_rows(lib, gpu):
+    # the 8192^3 scaled NN workload in the launch configuration the bench uses;
+    # the oracle computes 24 seeded rows plus the tile-seam rows in full
+    a, b, spec = synthetic.workload("c7")
+    c = synthetic.workload_c("c7")
+    d = lib.gemm_f16_scaled(_t(a, gpu), _t(b, gpu), _t(c, gpu), spec["alpha"], spec["beta"], "kn")
+    torch.cuda.synchronize()
+    got = d.cpu().numpy().view(np.uint16)
+    M = spec["M"]
+    u = synthetic.uniform01(3007, 24)
+    rows = sorted(set((u * M).astype(int).tolist()) | {0, 127, 128, 255, 256, M - 1})
+    ref = oracle.gemm_scaled(a[rows], b, c[rows], spec["alpha"], spec["beta"], True)
+    st = compare_scaled(got[rows], ref, spec["K"], a, b, c, spec["alpha"], spec["beta"])
+    assert st["bad"] == 0, st
+    assert np.isfinite(got.view(np.float16)).all()

@@ -14,6 +14,8 @@ with gcc into ``oracle/_build/`` and exposes it through ctypes:
   written from the IEEE 754 binary16 definition.
 * ``gemm_tn(a_bits, b_bits, threads)`` -- the full M x N product.
 * ``gemm_tn_sampled(a_bits, b_bits, rows, cols)`` -- selected elements.
+* ``gemm_tn_f16acc(a_bits, b_bits)`` -- the product with an fp16 accumulator
+  rounded after every 16-deep K slice (the page's MMA atom).
 * ``gemm_scaled(a_bits, b_bits, c_bits, alpha, beta, b_kn)`` -- the scaled
   form alpha * A op(B) + beta * C, with B N x K (TN) or K x N (NN).
 * ``minimum_stages(copy, compute)`` -- S_min = ceil(copy/compute) + 1
@@ -61,6 +63,8 @@ def _bind(lib):
     lib.oracle_gemm_scaled.argtypes = [u16p, u16p, u16p, u16p, i64, i64, i64, ctypes.c_float,
                                        ctypes.c_float, ctypes.c_int, ctypes.c_int]
     lib.oracle_gemm_scaled.restype = ctypes.c_int
+    lib.oracle_gemm_tn_f16acc.argtypes = [u16p, u16p, u16p, i64, i64, i64, ctypes.c_int]
+    lib.oracle_gemm_tn_f16acc.restype = ctypes.c_int
     lib.oracle_minimum_stages.argtypes = [i64, i64]
     lib.oracle_minimum_stages.restype = ctypes.c_int64
     return lib
@@ -133,6 +137,23 @@ def gemm_tn(a_bits: np.ndarray, b_bits: np.ndarray, threads: int | None = None, 
                                 _ptr(d, ctypes.c_uint16), M, N, K, threads or default_threads())
     if rc != 0:
         raise ValueError("oracle_gemm_tn rejected its arguments")
+    return d
+
+
+def gemm_tn_f16acc(a_bits: np.ndarray, b_bits: np.ndarray, threads: int | None = None,
+                   lib=None) -> np.ndarray:
+    """D = A B^T with an fp16 accumulator rounded after every 16-deep K slice."""
+    a, b = _u16(a_bits), _u16(b_bits)
+    if a.ndim != 2 or b.ndim != 2 or a.shape[1] != b.shape[1]:
+        raise ValueError("A must be M x K and B N x K")
+    M, K = a.shape
+    N = b.shape[0]
+    d = np.zeros((M, N), dtype=np.uint16)
+    rc = (lib or _load()).oracle_gemm_tn_f16acc(_ptr(a, ctypes.c_uint16), _ptr(b, ctypes.c_uint16),
+                                               _ptr(d, ctypes.c_uint16), M, N, K,
+                                               threads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_gemm_tn_f16acc rejected its arguments")
     return d
 
 

@@ -219,6 +219,71 @@ int oracle_gemm_scaled(const uint16_t* A, const uint16_t* B, const uint16_t* C, 
     return 0;
 }
 
+/* ---- fp16 accumulation ---------------------------------------------------
+ *
+ * "cute(9) multistage_gemm" builds its kernel on an MMA atom whose
+ * accumulator is fp16 (SM80_16x8x16_F16F16F16F16_TN in its config listing):
+ * every instruction adds a 16-deep slice of the K sum to an fp16
+ * accumulator and rounds the result to fp16.  Written out with the slice's
+ * products summed exactly:
+ *
+ *   acc = 0;  for each slice c of 16 consecutive k:
+ *       acc = fp16_rne( acc + sum_{k in c} double(A[i][k]) * double(B[j][k]) )
+ *   D[i][j] = acc
+ *
+ * (TN layout as oracle_gemm_tn; a last slice shorter than 16 when K is not
+ * a multiple of 16.) */
+static void* run_f16acc_rows(void* p)
+{
+    rows_job* j = (rows_job*)p;
+    for (int64_t i = j->row_begin; i < j->row_end; ++i) {
+        for (int64_t n = 0; n < j->N; ++n) {
+            const uint16_t* a_row = j->A + i * j->K;
+            const uint16_t* b_row = j->B + n * j->K;
+            double acc = 0.0;
+            for (int64_t k0 = 0; k0 < j->K; k0 += 16) {
+                double s = acc;
+                for (int64_t k = k0; k < k0 + 16 && k < j->K; ++k)
+                    s += oracle_half_to_double(a_row[k]) * oracle_half_to_double(b_row[k]);
+                acc = oracle_half_to_double(oracle_double_to_half(s));
+            }
+            j->D[i * j->N + n] = oracle_double_to_half(acc);
+        }
+    }
+    return NULL;
+}
+
+int oracle_gemm_tn_f16acc(const uint16_t* A, const uint16_t* B, uint16_t* D,
+                          int64_t M, int64_t N, int64_t K, int threads)
+{
+    enum { MAX_THREADS = 256 };
+    if (M < 0 || N < 0 || K < 0 || (M * N > 0 && (!A || !B || !D))) return -1;
+    if (M == 0 || N == 0) return 0;
+    if (threads < 1) threads = 1;
+    if (threads > MAX_THREADS) threads = MAX_THREADS;
+    if (threads > M) threads = (int)M;
+    pthread_t tid[MAX_THREADS];
+    int joined[MAX_THREADS];
+    rows_job job[MAX_THREADS];
+    int64_t per = (M + threads - 1) / threads;
+    for (int t = 0; t < threads; ++t) {
+        int64_t b = t * per, e = (t + 1) * per;
+        if (b > M) b = M;
+        if (e > M) e = M;
+        job[t] = (rows_job){A, B, D, M, N, K, b, e};
+        joined[t] = 0;
+    }
+    for (int t = 1; t < threads; ++t) {
+        if (job[t].row_begin >= job[t].row_end) continue;
+        if (pthread_create(&tid[t], NULL, run_f16acc_rows, &job[t]) == 0) joined[t] = 1;
+        else run_f16acc_rows(&job[t]);
+    }
+    run_f16acc_rows(&job[0]);
+    for (int t = 1; t < threads; ++t)
+        if (joined[t]) pthread_join(tid[t], NULL);
+    return 0;
+}
+
 /* Selected elements only: out[s] = D[rows[s]][cols[s]].  Used where the full
  * product is too large for the CPU (the 8192^3 case). */
 int oracle_gemm_tn_sampled(const uint16_t* A, const uint16_t* B,

@@ -13,7 +13,10 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 MUTANTS = {
     "drop_first_term": ("for (int64_t k = 0; k < K; ++k)", "for (int64_t k = 1; k < K; ++k)"),
-    "wrong_sign": ("s += oracle_half_to_double(a_row[k])", "s -= oracle_half_to_double(a_row[k])"),
+    "wrong_sign": ("    for (int64_t k = 0; k < K; ++k)\n        s += oracle_half_to_double(a_row[k])",
+                   "    for (int64_t k = 0; k < K; ++k)\n        s -= oracle_half_to_double(a_row[k])"),
+    "f16acc_wrong_sign": ("k < k0 + 16 && k < j->K; ++k)\n                    s += ",
+                          "k < k0 + 16 && k < j->K; ++k)\n                    s -= "),
     "transposed_result": ("dot_row_row(j->A + i * j->K, j->B + n * j->K, j->K)",
                           "dot_row_row(j->A + (n % j->M) * j->K, j->B + (i % j->N) * j->K, j->K)"),
     "b_row_from_i": ("j->B + n * j->K, j->K)", "j->B + (i % j->N) * j->K, j->K)"),
@@ -34,6 +37,9 @@ MUTANTS = {
     "scaled_alpha_skipped": ("double v = j->alpha * s;", "double v = s;"),
     "scaled_nn_read_as_tn": ("j->b_kn ? j->B[k * j->N + n] : j->B[n * j->K + k]",
                              "j->b_kn ? j->B[(n * j->K + k) % (j->K * j->N)] : j->B[n * j->K + k]"),
+    "f16acc_slice_32": ("for (int64_t k0 = 0; k0 < j->K; k0 += 16) {", "for (int64_t k0 = 0; k0 < j->K; k0 += 32) {"),
+    "f16acc_inner_32": ("k < k0 + 16 && k < j->K", "k < k0 + 32 && k < j->K"),
+    "f16acc_no_slice_rounding": ("acc = oracle_half_to_double(oracle_double_to_half(s));", "acc = s;"),
     "scaled_beta_on_alpha": ("v += j->beta * oracle_half_to_double", "v += j->alpha * oracle_half_to_double"),
 }
 

@@ -385,3 +385,64 @@ def test_scaled_special_cases():
                           oracle.gemm_scaled(a, b_nk, c, 0.8, -0.3, False))
     assert np.array_equal(oracle.gemm_scaled(a, b_nk, None, 1.0, 0.0, False),
                           oracle.gemm_tn(a, b_nk))
+
+
+# --------------------------------------------------------------------------- fp16 accumulation
+# "cute(9) multistage_gemm": its MMA atom accumulates in fp16, one rounding per
+# 16-deep K slice.
+def _f16acc_reference(a_bits, b_bits):
+    """The slice-by-slice rounding written with exact rationals."""
+    a = a_bits.view(np.float16).astype(np.float64)
+    b = b_bits.view(np.float16).astype(np.float64)
+    M, K = a.shape
+    N = b.shape[0]
+    out = np.zeros((M, N), dtype=np.uint16)
+    for i in range(M):
+        for j in range(N):
+            acc = Fraction(0)
+            for k0 in range(0, K, 16):
+                s = acc + sum(Fraction(a[i, k]) * Fraction(b[j, k]) for k in range(k0, min(K, k0 + 16)))
+                bits = _fraction_to_half_bits(s)
+                acc = Fraction(float(np.uint16(bits).view(np.float16)))
+            out[i, j] = _fraction_to_half_bits(acc)
+    return out
+
+
+def test_f16acc_loses_what_an_fp16_accumulator_loses():
+    # slice 1 sums to 2048; slices 2 and 3 each add 1.  In fp16, 2049 is a tie
+    # between 2048 and 2050 and goes to the even 2048, so each added 1 is lost
+    # and D = 2048, where the exactly summed product is 2050.
+    K = 48
+    a = np.zeros((1, K)); b = np.zeros((1, K))
+    a[0, :16] = 128.0; b[0, :16] = 1.0          # 16 * 128 = 2048
+    a[0, 16] = 1.0; b[0, 16] = 1.0              # + 1 in slice 2
+    a[0, 32] = 1.0; b[0, 32] = 1.0              # + 1 in slice 3
+    ah = a.astype(np.float16).view(np.uint16); bh = b.astype(np.float16).view(np.uint16)
+    assert float(oracle.gemm_tn_f16acc(ah, bh).view(np.float16)[0, 0]) == 2048.0
+    assert float(oracle.gemm_tn(ah, bh).view(np.float16)[0, 0]) == 2050.0
+
+
+def test_f16acc_single_slice_is_one_rounding():
+    # K <= 16: one slice, so fp16 accumulation is the plain product, rounded once
+    rng = np.random.default_rng(41)
+    for K in (1, 8, 16):
+        a = rng.uniform(-1, 1, (6, K)).astype(np.float16).view(np.uint16)
+        b = rng.uniform(-1, 1, (5, K)).astype(np.float16).view(np.uint16)
+        assert np.array_equal(oracle.gemm_tn_f16acc(a, b), oracle.gemm_tn(a, b))
+
+
+def test_f16acc_integer_sums_are_exact():
+    # {-1,0,1} at K = 1024: every partial sum is an integer of magnitude <= 1024,
+    # exact in fp16, so slice-wise rounding changes nothing
+    a = synthetic.ternary(51, (24, 1024))
+    b = synthetic.ternary(52, (20, 1024))
+    ai = a.view(np.float16).astype(np.int64); bi = b.view(np.float16).astype(np.int64)
+    assert np.array_equal(oracle.gemm_tn_f16acc(a, b), (ai @ bi.T).astype(np.float16).view(np.uint16))
+
+
+@pytest.mark.parametrize("K", [17, 40, 100])
+def test_f16acc_random_against_exact_slices(K):
+    rng = np.random.default_rng(K)
+    a = rng.uniform(-2, 2, (4, K)).astype(np.float16).view(np.uint16)
+    b = rng.uniform(-2, 2, (3, K)).astype(np.float16).view(np.uint16)
+    assert np.array_equal(oracle.gemm_tn_f16acc(a, b), _f16acc_reference(a, b))

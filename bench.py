@@ -294,8 +294,9 @@ def run_gpu(args, tag):
         if scaled:
             return binding.gemm_f16_scaled(a_, b_, c_, spec["alpha"], spec["beta"],
                                            "kn" if b_kn else "nk", out=d_, stream=st, **opts)
-        if forced:
-            return binding.gemm_tn_f16_ex(a_, b_, out=d_, stream=st, **opts)
+        if forced or spec.get("acc_f16"):
+            return binding.gemm_tn_f16_ex(a_, b_, out=d_, stream=st,
+                                          acc_f16=1 if spec.get("acc_f16") else 0, **opts)
         return binding.gemm_tn_f16(a_, b_, out=d_, stream=st)
 
     def launch(i):
@@ -459,7 +460,8 @@ def run_gpu(args, tag):
     line = {"metric": METRIC, "value": job_throughput(flops, world, ms) / 1e12, "unit": UNIT,
             "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f16 (fp16 accumulator)" if spec.get("acc_f16") else "f16",
             "data": "synthetic (seeded splitmix64, fp16-rounded)",
             "config": workload_config(tag, spec, {
                 "l2": (f"inputs larger than L2: {R} copies of A, B, D ({R * per_copy >> 20} MiB "

@@ -86,6 +86,9 @@ typedef struct {
                           TMEM -> global drain rate, for short k loops) */
   int b_layout;        /* gemm_query_config only: plan for this B layout (GEMM_B_*);
                           gemm_f16_scaled takes the layout as an argument */
+  int acc_f16;         /* 0: fp32 accumulator (default); 1: fp16 accumulator, rounded
+                          after every 16-deep K slice -- the arithmetic of the
+                          F16F16F16F16 MMA atom of "cute(9) multistage_gemm" */
 } gemm_options_t;
 
 /* gemm_tn_f16 with an explicit configuration (sweeps, tests).  Same

@@ -235,6 +235,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(leader_tempty);
         }
+        if (p.acc_f16) widen_f16_accumulator(r);
         if (p.scaled) apply_alpha_beta(r, p, m0 + lane, n0 + c * kEpiCols);
         const uint32_t buf = my_bufs + (chunk_seq % kEpiBufs) * kEpiChunkBytes;
         if (chunk_seq >= static_cast<uint32_t>(kEpiBufs)) {

@@ -131,7 +131,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   if (opt) o = *opt;
   if (o.path < 0 || o.path > 3 || o.bn < 0 || o.bn > 256 || (o.bn % 32) != 0 || o.kstage < 0 ||
       o.kstage == 1 || o.kstage > kMaxStages || o.max_ctas < 0 || o.group_m < 0 || o.inject < 0 ||
-      o.inject > 1 || o.katoms < 0 || o.katoms > 2 ||
+      o.inject > 1 || o.katoms < 0 || o.katoms > 2 || o.acc_f16 < 0 || o.acc_f16 > 1 ||
       (o.epi_warps != 0 && o.epi_warps != 4 && o.epi_warps != 8))
     return GEMM_ERR_INVALID_VALUE;
   if (o.path == GEMM_PATH_SKINNY && M > kBM) return GEMM_ERR_INVALID_VALUE;
@@ -235,6 +235,8 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   p.num_tiles = static_cast<int32_t>(tiles);
   p.group_m = group_m;
   p.idesc = make_idesc(bm, bn) | (b_kn ? (1u << 16) : 0u);  // bit 16: B is MN-major
+  if (o.acc_f16) p.idesc &= ~(3u << 4);                      // bits 4-5: D format F16
+  p.acc_f16 = o.acc_f16;
   p.b_kn = b_kn;
   p.tmem_cols = pow2_at_least(2u * bn);
   p.stage_bytes = stage_bytes;

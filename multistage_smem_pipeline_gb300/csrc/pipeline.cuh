@@ -46,6 +46,7 @@ struct GemmParams {
   int32_t scaled;        // 1: D = alpha * acc + beta * C instead of D = acc
   float alpha, beta;
   const uint16_t* C;     // M x N fp16, row stride N; read only when scaled and beta != 0
+  int32_t acc_f16;       // 1: fp16 accumulator (low 16 bits of each TMEM column)
 };
 
 // MN-major B: one 64-element N chunk per TMA box; chunks 8 KiB apart.
@@ -108,6 +109,14 @@ __device__ __forceinline__ void tile_coords(int t, const GemmParams& p, int& mb,
 __device__ __forceinline__ uint32_t pack_half2(uint32_t lo_bits, uint32_t hi_bits) {
   const __half2 h = __floats2half2_rn(__uint_as_float(lo_bits), __uint_as_float(hi_bits));
   return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// An fp16 accumulator occupies the low 16 bits of each 32-bit TMEM column;
+// widen it to fp32 bits (exactly) so the rest of the epilogue is shared.
+__device__ __forceinline__ void widen_f16_accumulator(uint32_t (&r)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    r[i] = __float_as_uint(__half2float(__ushort_as_half(static_cast<unsigned short>(r[i]))));
 }
 
 // r (fp32 bits of one row's 32 accumulator columns) <- alpha * r + beta * C

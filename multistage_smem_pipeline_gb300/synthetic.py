@@ -26,6 +26,9 @@ c6     81920 x 256 x 256        U[-1, 1] (the tall shape "cute(9)
 c7     8192 x 8192 x 8192       U[-1, 1]; the scaled NN form of "CUDA 算子笔记
                                 2" (GEMM section): D = 1.5 A B - 0.5 C with
                                 B K x N and C U[-1, 1]
+c8     81920 x 256 x 256        U[-1, 1] with an fp16 accumulator: the shape
+                                and the accumulator of the page's own
+                                measurement ("cute(9)", section 11)
 =====  =======================  ===========================================
 """
 from __future__ import annotations
@@ -100,6 +103,7 @@ WORKLOADS = {
     "c5": dict(M=128, N=14336, K=4096, kind="skinny"),
     "c6": dict(M=81920, N=256, K=256, kind="uniform"),
     "c7": dict(M=8192, N=8192, K=8192, kind="uniform", b_kn=True, alpha=1.5, beta=-0.5),
+    "c8": dict(M=81920, N=256, K=256, kind="uniform", acc_f16=True),
 }
 WORKLOAD_NAMES = {
     "c1": "gemm_tn_f16 256x256x256 U[-1,1]",
@@ -109,11 +113,12 @@ WORKLOAD_NAMES = {
     "c5": "gemm_tn_f16 skinny M=128 N=14336 K=4096 A~N(0,1) B~N(0,0.02)",
     "c6": "gemm_tn_f16 tall M=81920 N=256 K=256 U[-1,1]",
     "c7": "gemm_f16_scaled NN 8192x8192x8192 D=1.5*A*B-0.5*C U[-1,1]",
+    "c8": "gemm_tn_f16 tall M=81920 N=256 K=256 U[-1,1], fp16 accumulator",
 }
 
 
 def seeds(tag: str) -> tuple[int, int, int]:
-    """(seed_A, seed_B, seed_samples) for a workload tag c1..c7."""
+    """(seed_A, seed_B, seed_samples) for a workload tag c1..c8."""
     c = int(tag[1:])
     return 1000 + c, 2000 + c, 3000 + c
 
@@ -133,7 +138,7 @@ def make_operands(kind: str, M: int, N: int, K: int, seed_a: int, seed_b: int):
 
 
 def workload(tag: str):
-    """(A_bits, B_bits, spec) for a workload tag c1..c7.  B is N x K, or K x N
+    """(A_bits, B_bits, spec) for a workload tag c1..c8.  B is N x K, or K x N
     where spec["b_kn"] is set."""
     spec = WORKLOADS[tag]
     sa, sb, _ = seeds(tag)

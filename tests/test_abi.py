@@ -99,7 +99,8 @@ def test_empty_output_is_a_noop_without_device(binding):
 def test_rejects_bad_options(binding):
     for kw in [dict(bn=48), dict(bn=512), dict(kstage=1), dict(kstage=17), dict(path=4),
                dict(inject=2), dict(max_ctas=-1), dict(path=binding.PATH_SKINNY),
-               dict(katoms=3), dict(katoms=-1), dict(epi_warps=6), dict(epi_warps=16)]:
+               dict(katoms=3), dict(katoms=-1), dict(epi_warps=6), dict(epi_warps=16),
+               dict(acc_f16=2)]:
         o = binding._options(**kw)
         M = 256 if kw.get("path") == binding.PATH_SKINNY else 64
         assert _call(binding, P0, P1, P2, M, 64, 64, o) == binding.GEMM_ERR_INVALID_VALUE, kw

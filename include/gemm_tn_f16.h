@@ -126,6 +126,52 @@ int gemm_f16_scaled(void* D, const void* C, const void* A, const void* B, int64_
                     int64_t K, float alpha, float beta, int b_layout, const gemm_options_t* opt,
                     void* stream);
 
+/*
+ * gemm_f16_padded: gemm_f16_scaled for any K and N and any 2-byte-aligned
+ * operand -- the general shapes the host wrapper of "CUDA 算子笔记 2" (GEMM
+ * section) serves by copying A, B and C into zero-padded buffers before its
+ * kernel and copying the result back.
+ *
+ * Same operation, layouts (leading dimensions K or N, rows packed back to
+ * back) and ownership as gemm_f16_scaled.  Each operand whose base address
+ * or row stride is not a multiple of 16 bytes is first copied, on `stream`,
+ * into `workspace` with its rows padded to a multiple of 8 elements (+0 in
+ * the pad); the GEMM kernel then runs on the aligned copies, and a padded D
+ * is copied back into D.  Operands already aligned are used in place, so
+ * with K % 8 == 0, N % 8 == 0 and 16-byte-aligned pointers this is exactly
+ * gemm_f16_scaled and needs no workspace.  The results are those of the
+ * unpadded problem: the pad contributes exact zeros.
+ *
+ *   workspace        device, caller-owned, 16-byte aligned, at least the
+ *                    size gemm_padded_workspace_bytes returns for the same
+ *                    D, C, A, B, M, N, K, beta and b_layout; it must not
+ *                    overlap any operand.  Its contents on entry do not
+ *                    matter and on return are unspecified.  It may be NULL
+ *                    when that size is 0.  Calls in flight at once on
+ *                    different streams need separate workspaces.
+ *   workspace_bytes  its size in bytes.
+ *
+ * Errors: a pointer that is odd (not fp16-aligned) is GEMM_ERR_MISALIGNED;
+ * a workspace that is too small or overlaps an operand is
+ * GEMM_ERR_INVALID_VALUE, and a misaligned one GEMM_ERR_MISALIGNED; the
+ * other checks are those of gemm_f16_scaled.  Nothing is launched when a
+ * check fails.  Up to four kernels are launched (repack A, repack B, the
+ * GEMM -- after a repack of C where C is read -- and the copy back of D),
+ * all asynchronous on `stream`.
+ */
+int gemm_f16_padded(void* D, const void* C, const void* A, const void* B, int64_t M, int64_t N,
+                    int64_t K, float alpha, float beta, int b_layout, void* workspace,
+                    uint64_t workspace_bytes, const gemm_options_t* opt, void* stream);
+
+/* Workspace bytes gemm_f16_padded needs for these arguments (0 when every
+ * operand it reads or writes is already aligned).  It depends on the
+ * pointers' alignment, so pass the pointers of the call (they are not
+ * dereferenced).  Host only; returns GEMM_ERR_INVALID_VALUE for a negative
+ * or too-large size, a bad b_layout or a NULL `bytes`. */
+int gemm_padded_workspace_bytes(const void* D, const void* C, const void* A, const void* B,
+                                int64_t M, int64_t N, int64_t K, float beta, int b_layout,
+                                uint64_t* bytes);
+
 /* Chosen configuration for a shape (host only, no GPU work; needs a current
  * device only to read its SM count -- with no device, 148 SMs are assumed). */
 typedef struct {

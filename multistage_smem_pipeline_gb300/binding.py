@@ -25,8 +25,8 @@ PATH_AUTO, PATH_SQUARE, PATH_SKINNY, PATH_PAIR = 0, 1, 2, 3
 
 B_NK, B_KN = 0, 1
 
-EXPORTED = ("gemm_tn_f16", "gemm_tn_f16_ex", "gemm_f16_scaled", "gemm_query_config",
-            "gemm_get_device_error",
+EXPORTED = ("gemm_tn_f16", "gemm_tn_f16_ex", "gemm_f16_scaled", "gemm_f16_padded",
+            "gemm_padded_workspace_bytes", "gemm_query_config", "gemm_get_device_error",
             "gemm_minimum_stages", "gemm_probe_latencies", "gemm_probe_latencies_static",
             "gemm_status_string")
 
@@ -67,6 +67,12 @@ def _load() -> ctypes.CDLL:
     lib.gemm_f16_scaled.argtypes = [vp, vp, vp, vp, i64, i64, i64, ctypes.c_float, ctypes.c_float,
                                     i32, ctypes.POINTER(GemmOptions), vp]
     lib.gemm_f16_scaled.restype = i32
+    lib.gemm_f16_padded.argtypes = [vp, vp, vp, vp, i64, i64, i64, ctypes.c_float, ctypes.c_float,
+                                    i32, vp, ctypes.c_uint64, ctypes.POINTER(GemmOptions), vp]
+    lib.gemm_f16_padded.restype = i32
+    lib.gemm_padded_workspace_bytes.argtypes = [vp, vp, vp, vp, i64, i64, i64, ctypes.c_float, i32,
+                                                ctypes.POINTER(ctypes.c_uint64)]
+    lib.gemm_padded_workspace_bytes.restype = i32
     lib.gemm_query_config.argtypes = [i64, i64, i64, ctypes.POINTER(GemmOptions),
                                       ctypes.POINTER(GemmConfig)]
     lib.gemm_query_config.restype = i32
@@ -149,14 +155,8 @@ def gemm_tn_f16_ex(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = 
     return out
 
 
-def gemm_f16_scaled(a: torch.Tensor, b: torch.Tensor, c: torch.Tensor | None = None,
-                    alpha: float = 1.0, beta: float = 0.0, b_layout: str = "kn",
-                    out: torch.Tensor | None = None, stream=None, **opts) -> torch.Tensor:
-    """out = alpha * A @ op(B) + beta * C via the C-ABI (fp32 accumulate, fp16 out).
-
-    b_layout "kn": B is K x N (out = alpha A B + beta C); "nk": B is N x K
-    (out = alpha A B^T + beta C).  C is read only when beta != 0; passing
-    out=c updates C in place."""
+def _scaled_operands(a, b, c, out, b_layout: str, contiguous_what: str):
+    """Checks the tensors of the scaled form; returns (M, N, K, kn, out)."""
     if b_layout not in ("kn", "nk"):
         raise ValueError("b_layout must be 'kn' or 'nk'")
     kn = b_layout == "kn"
@@ -182,7 +182,19 @@ def gemm_f16_scaled(a: torch.Tensor, b: torch.Tensor, c: torch.Tensor | None = N
         out = torch.empty((M, N), dtype=torch.float16, device=a.device)
     elif out.dtype != torch.float16 or tuple(out.shape) != (M, N) or not out.is_contiguous() \
             or out.device != a.device:
-        raise ValueError("out must be a contiguous float16 M x N tensor on A's device")
+        raise ValueError(f"out must be a {contiguous_what} float16 M x N tensor on A's device")
+    return M, N, K, kn, out
+
+
+def gemm_f16_scaled(a: torch.Tensor, b: torch.Tensor, c: torch.Tensor | None = None,
+                    alpha: float = 1.0, beta: float = 0.0, b_layout: str = "kn",
+                    out: torch.Tensor | None = None, stream=None, **opts) -> torch.Tensor:
+    """out = alpha * A @ op(B) + beta * C via the C-ABI (fp32 accumulate, fp16 out).
+
+    b_layout "kn": B is K x N (out = alpha A B + beta C); "nk": B is N x K
+    (out = alpha A B^T + beta C).  C is read only when beta != 0; passing
+    out=c updates C in place."""
+    M, N, K, kn, out = _scaled_operands(a, b, c, out, b_layout, "contiguous")
     o = _options(**opts)
     with torch.cuda.device(a.device):
         rc = LIB.gemm_f16_scaled(out.data_ptr(), c.data_ptr() if c is not None else None,
@@ -190,6 +202,44 @@ def gemm_f16_scaled(a: torch.Tensor, b: torch.Tensor, c: torch.Tensor | None = N
                                  B_KN if kn else B_NK, ctypes.byref(o), _stream_handle(stream))
     if rc != GEMM_OK:
         raise GemmError(rc, "gemm_f16_scaled")
+    return out
+
+
+def padded_workspace_bytes(a: torch.Tensor, b: torch.Tensor, c: torch.Tensor | None,
+                           out: torch.Tensor, beta: float = 0.0, b_layout: str = "nk") -> int:
+    """Workspace bytes gemm_f16_padded needs for exactly these tensors."""
+    M, N, K, kn, out = _scaled_operands(a, b, c, out, b_layout, "contiguous")
+    n = ctypes.c_uint64(0)
+    rc = LIB.gemm_padded_workspace_bytes(out.data_ptr(), c.data_ptr() if c is not None else None,
+                                         a.data_ptr(), b.data_ptr(), M, N, K, float(beta),
+                                         B_KN if kn else B_NK, ctypes.byref(n))
+    if rc != GEMM_OK:
+        raise GemmError(rc, "gemm_padded_workspace_bytes")
+    return int(n.value)
+
+
+def gemm_f16_padded(a: torch.Tensor, b: torch.Tensor, c: torch.Tensor | None = None,
+                    alpha: float = 1.0, beta: float = 0.0, b_layout: str = "nk",
+                    out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                    stream=None, **opts) -> torch.Tensor:
+    """gemm_f16_scaled for any K and N (and any fp16-aligned tensors): operands
+    whose rows are not 16-byte aligned are repacked into `workspace` (a uint8
+    CUDA tensor; allocated here when None) before the GEMM kernel."""
+    M, N, K, kn, out = _scaled_operands(a, b, c, out, b_layout, "contiguous")
+    need = padded_workspace_bytes(a, b, c, out, beta, b_layout)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=a.device)
+    elif workspace.dtype != torch.uint8 or not workspace.is_contiguous() \
+            or workspace.device != a.device:
+        raise ValueError("workspace must be a contiguous uint8 tensor on A's device")
+    o = _options(**opts)
+    with torch.cuda.device(a.device):
+        rc = LIB.gemm_f16_padded(out.data_ptr(), c.data_ptr() if c is not None else None,
+                                 a.data_ptr(), b.data_ptr(), M, N, K, float(alpha), float(beta),
+                                 B_KN if kn else B_NK, workspace.data_ptr(), workspace.numel(),
+                                 ctypes.byref(o), _stream_handle(stream))
+    if rc != GEMM_OK:
+        raise GemmError(rc, "gemm_f16_padded")
     return out
 
 

@@ -13,6 +13,7 @@
 
 #include "gemm_pair_kernel.cuh"
 #include "gemm_tn_f16.h"
+#include "repack.cuh"
 
 namespace gb300 {
 namespace {
@@ -253,13 +254,21 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   return GEMM_OK;
 }
 
-int encode_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
-              uint32_t box_outer, CUtensorMapSwizzle swz) {
-  const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {inner * 2};  // bytes between rows
+// A row-major fp16 matrix as one TMA tensor map sees it: `cols` contiguous
+// elements per row, `rows` rows, `ld` elements between row starts (ld * 2 a
+// multiple of 16, the base 16-byte aligned).
+struct View {
+  const void* ptr;
+  uint64_t cols, rows, ld;
+};
+
+int encode_2d(CUtensorMap* map, const View& v, uint32_t box_inner, uint32_t box_outer,
+              CUtensorMapSwizzle swz) {
+  const cuuint64_t dims[2] = {v.cols, v.rows};
+  const cuuint64_t strides[1] = {v.ld * 2};  // bytes between rows
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr),
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(v.ptr),
                               dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -356,42 +365,39 @@ int check_scaled(const void* D, const Scaled& sc, int64_t M, int64_t N) {
   return GEMM_OK;
 }
 
-int run(void* D, const void* A, const void* B, int64_t M, int64_t N, int64_t K,
-        const gemm_options_t* opt, cudaStream_t stream, const Scaled* sc = nullptr) {
-  int rc = check_args(D, A, B, M, N, K);
-  if (rc != GEMM_OK) return rc;
-  const int b_kn = sc ? sc->b_kn : 0;
-  if (sc && (rc = check_scaled(D, *sc, M, N)) != GEMM_OK) return rc;
-  if (opt) {  // validate options even when there is nothing to compute
-    Plan tmp;
-    rc = make_plan(std::max<int64_t>(M, 1), std::max<int64_t>(N, 8), std::max<int64_t>(K, 8), opt,
-                   148, 74, &tmp, b_kn);
-    if (rc != GEMM_OK) return rc;
+// D = beta * C (rounded to fp16), or D = 0 when beta == 0: the empty sum
+// (K == 0).  Element by element, so any 2-byte alignment is accepted.
+int write_empty_sum(void* D, const void* C, float beta, int64_t n, int sm_count,
+                    cudaStream_t stream) {
+  if (C && beta != 0.0f) {
+    const int blocks = static_cast<int>(std::min<int64_t>((n + 255) / 256, 8 * sm_count));
+    scale_c_kernel<<<blocks, 256, 0, stream>>>(static_cast<uint16_t*>(D),
+                                               static_cast<const uint16_t*>(C), beta, n);
+    return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
   }
-  if (M == 0 || N == 0) return GEMM_OK;
-  int dev = 0;
-  DeviceState* st = nullptr;
-  rc = current_device(&dev, &st);
-  if (rc != GEMM_OK) return rc;
-  if (K == 0) {  // the empty sum: D = 0, or D = beta * C in the scaled form
-    if (sc && sc->beta != 0.0f) {
-      const int64_t n = M * N;
-      const int blocks = static_cast<int>(std::min<int64_t>((n + 255) / 256, 8 * st->sm_count));
-      scale_c_kernel<<<blocks, 256, 0, stream>>>(static_cast<uint16_t*>(D),
-                                                 static_cast<const uint16_t*>(sc->C), sc->beta, n);
-      return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
-    }
-    if (cudaMemsetAsync(D, 0, static_cast<size_t>(M) * N * 2, stream) != cudaSuccess) {
-      cudaGetLastError();
-      return GEMM_ERR_CUDA;
-    }
-    return GEMM_OK;
+  if (cudaMemsetAsync(D, 0, static_cast<size_t>(n) * 2, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
   }
+  return GEMM_OK;
+}
+
+// One GEMM launch on aligned operands.  M, N, K are the extents the kernel
+// tiles and iterates; the views give each operand's tensor-map extents and
+// row stride (A: K x M, B: K x N for an N x K B or N x K for a K x N B,
+// D: N x M, as cols x rows).  A view may be narrower than the iterated
+// extent: the loads past its edge read zeros.  sc != nullptr selects the
+// scaled epilogue, reading C with row stride ldc.
+int launch_gemm(int64_t M, int64_t N, int64_t K, const View& a, const View& b, const View& d,
+                int b_kn, const Scaled* sc, int64_t ldc, const gemm_options_t* opt,
+                DeviceState* st, cudaStream_t stream) {
+  int rc;
   if ((rc = prepare_device(st)) != GEMM_OK) return rc;
   Plan pl;
   rc = make_plan(M, N, K, opt, st->sm_count, st->max_pairs, &pl, b_kn);
   if (rc != GEMM_OK) return rc;
   if ((rc = get_encoder()) != GEMM_OK) return rc;
+  pl.p.ldc = ldc;
   if (sc && !(sc->alpha == 1.0f && sc->beta == 0.0f)) {
     pl.p.scaled = 1;
     pl.p.alpha = sc->alpha;
@@ -402,11 +408,10 @@ int run(void* D, const void* A, const void* B, int64_t M, int64_t N, int64_t K,
   const bool pair = pl.cfg.path == GEMM_PATH_PAIR;
   const uint32_t b_box_rows = pair ? pl.cfg.bn / 2 : pl.cfg.bn;
   CUtensorMap tmA, tmB, tmD;
-  const int b_rc = b_kn ? encode_2d(&tmB, B, N, K, 64, kBK, CU_TENSOR_MAP_SWIZZLE_128B)
-                        : encode_2d(&tmB, B, K, N, kBK, b_box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
-  if (encode_2d(&tmA, A, K, M, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B) != GEMM_OK ||
-      b_rc != GEMM_OK ||
-      encode_2d(&tmD, D, N, M, kEpiCols, 32, CU_TENSOR_MAP_SWIZZLE_64B) != GEMM_OK)
+  const int b_rc = b_kn ? encode_2d(&tmB, b, 64, kBK, CU_TENSOR_MAP_SWIZZLE_128B)
+                        : encode_2d(&tmB, b, kBK, b_box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (encode_2d(&tmA, a, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B) != GEMM_OK || b_rc != GEMM_OK ||
+      encode_2d(&tmD, d, kEpiCols, 32, CU_TENSOR_MAP_SWIZZLE_64B) != GEMM_OK)
     return GEMM_ERR_INVALID_VALUE;
 
   const int threads = threads_for(pl.cfg.epi_warps);
@@ -443,6 +448,164 @@ int run(void* D, const void* A, const void* B, int64_t M, int64_t N, int64_t K,
   return GEMM_OK;
 }
 
+// Options are checked against the shape even when there is nothing to compute.
+int check_options(const gemm_options_t* opt, int b_kn, int64_t M, int64_t N, int64_t K) {
+  if (!opt) return GEMM_OK;
+  Plan tmp;
+  return make_plan(std::max<int64_t>(M, 1), std::max<int64_t>(N, 8), std::max<int64_t>(K, 8), opt,
+                   148, 74, &tmp, b_kn);
+}
+
+int run(void* D, const void* A, const void* B, int64_t M, int64_t N, int64_t K,
+        const gemm_options_t* opt, cudaStream_t stream, const Scaled* sc = nullptr) {
+  int rc = check_args(D, A, B, M, N, K);
+  if (rc != GEMM_OK) return rc;
+  const int b_kn = sc ? sc->b_kn : 0;
+  if (sc && (rc = check_scaled(D, *sc, M, N)) != GEMM_OK) return rc;
+  if ((rc = check_options(opt, b_kn, M, N, K)) != GEMM_OK) return rc;
+  if (M == 0 || N == 0) return GEMM_OK;
+  int dev = 0;
+  DeviceState* st = nullptr;
+  rc = current_device(&dev, &st);
+  if (rc != GEMM_OK) return rc;
+  if (K == 0)
+    return write_empty_sum(D, sc ? sc->C : nullptr, sc ? sc->beta : 0.0f, M * N, st->sm_count,
+                           stream);
+  const uint64_t m = M, n = N, k = K;
+  const View a{A, k, m, k};
+  const View b = b_kn ? View{B, n, k, n} : View{B, k, n, k};
+  const View d{D, n, m, n};
+  return launch_gemm(M, N, K, a, b, d, b_kn, sc, N, opt, st, stream);
+}
+
+// ---------------------------------------------------------------- padded path
+//
+// Any K and N and any 2-byte-aligned operand: every operand whose base or
+// row stride is not 16-byte aligned is first copied into a caller-owned
+// workspace with rows padded to a multiple of 8 elements (+0 in the pad),
+// the GEMM runs on the aligned copies, and D is copied back.  This is the
+// host wrapper of "CUDA 算子笔记 2" (GEMM section), which pads A, B and C to
+// tile multiples before its kernel; here the pad is only what TMA needs.
+
+struct PadPlan {
+  int64_t Kp, Np;
+  bool pack_a, pack_b, pad_d;
+  bool c_to_d;          // C copied into D (D aligned, C not); then C := D (in place)
+  uint64_t off_a, off_b, off_d, total;
+};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+uint64_t round_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
+
+// Which operands are repacked and where they go in the workspace.  The pure
+// function of the arguments that both gemm_padded_workspace_bytes and
+// gemm_f16_padded evaluate.
+PadPlan plan_padding(const void* D, const void* C, const void* A, const void* B, int64_t M,
+                     int64_t N, int64_t K, float beta, int b_kn) {
+  PadPlan pp;
+  std::memset(&pp, 0, sizeof(pp));
+  pp.Kp = padded_cols(K);
+  pp.Np = padded_cols(N);
+  if (M == 0 || N == 0 || K == 0) return pp;  // nothing reaches the GEMM kernel
+  pp.pack_a = !aligned16(A) || K % 8 != 0;
+  pp.pack_b = !aligned16(B) || (b_kn ? N % 8 != 0 : K % 8 != 0);
+  pp.pad_d = !aligned16(D) || N % 8 != 0;
+  pp.c_to_d = !pp.pad_d && beta != 0.0f && !aligned16(C);
+  constexpr uint64_t kRegionAlign = 256;
+  uint64_t off = 0;
+  if (pp.pack_a) {
+    pp.off_a = off;
+    off += round_up(static_cast<uint64_t>(M) * pp.Kp * 2, kRegionAlign);
+  }
+  if (pp.pack_b) {
+    pp.off_b = off;
+    off += round_up(b_kn ? static_cast<uint64_t>(K) * pp.Np * 2
+                         : static_cast<uint64_t>(N) * pp.Kp * 2,
+                    kRegionAlign);
+  }
+  if (pp.pad_d) {
+    pp.off_d = off;
+    off += round_up(static_cast<uint64_t>(M) * pp.Np * 2, kRegionAlign);
+  }
+  pp.total = off;
+  return pp;
+}
+
+int check_padded_args(const void* D, const void* C, const void* A, const void* B, int64_t M,
+                      int64_t N, int64_t K, float alpha, float beta, int b_kn) {
+  if (M < 0 || N < 0 || K < 0 || M > INT_MAX || N > INT_MAX || K > INT_MAX)
+    return GEMM_ERR_INVALID_VALUE;
+  if (b_kn != 0 && b_kn != 1) return GEMM_ERR_INVALID_VALUE;
+  if (!std::isfinite(alpha) || !std::isfinite(beta)) return GEMM_ERR_INVALID_VALUE;
+  if (M == 0 || N == 0) return GEMM_OK;
+  if (!D || (K > 0 && (!A || !B)) || (beta != 0.0f && !C)) return GEMM_ERR_INVALID_VALUE;
+  const auto odd = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 1) != 0; };
+  if (odd(D) || (K > 0 && (odd(A) || odd(B))) || (beta != 0.0f && odd(C)))
+    return GEMM_ERR_MISALIGNED;
+  const uint64_t dbytes = static_cast<uint64_t>(M) * N * 2;
+  if (K > 0 && (overlaps(D, dbytes, A, static_cast<uint64_t>(M) * K * 2) ||
+                overlaps(D, dbytes, B, static_cast<uint64_t>(N) * K * 2)))
+    return GEMM_ERR_INVALID_VALUE;
+  if (beta != 0.0f && C != D && overlaps(C, dbytes, D, dbytes)) return GEMM_ERR_INVALID_VALUE;
+  return GEMM_OK;
+}
+
+int run_padded(void* D, const void* C, const void* A, const void* B, int64_t M, int64_t N,
+               int64_t K, float alpha, float beta, int b_kn, void* workspace,
+               uint64_t workspace_bytes, const gemm_options_t* opt, cudaStream_t stream) {
+  int rc = check_padded_args(D, C, A, B, M, N, K, alpha, beta, b_kn);
+  if (rc != GEMM_OK) return rc;
+  if ((rc = check_options(opt, b_kn, M, N, K)) != GEMM_OK) return rc;
+  if (M == 0 || N == 0) return GEMM_OK;
+  const PadPlan pp = plan_padding(D, C, A, B, M, N, K, beta, b_kn);
+  if (pp.total > 0) {
+    if (!workspace || workspace_bytes < pp.total) return GEMM_ERR_INVALID_VALUE;
+    if (!aligned16(workspace)) return GEMM_ERR_MISALIGNED;
+    const uint64_t dbytes = static_cast<uint64_t>(M) * N * 2;
+    if (overlaps(workspace, pp.total, D, dbytes) ||
+        (beta != 0.0f && overlaps(workspace, pp.total, C, dbytes)) ||
+        (K > 0 && (overlaps(workspace, pp.total, A, static_cast<uint64_t>(M) * K * 2) ||
+                   overlaps(workspace, pp.total, B, static_cast<uint64_t>(N) * K * 2))))
+      return GEMM_ERR_INVALID_VALUE;
+  }
+  int dev = 0;
+  DeviceState* st = nullptr;
+  if ((rc = current_device(&dev, &st)) != GEMM_OK) return rc;
+  if (K == 0) return write_empty_sum(D, C, beta, M * N, st->sm_count, stream);
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const int sms = st->sm_count;
+  const auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+  if (pp.pack_a && !ok(repack_rows(ws + pp.off_a, A, M, K, sms, stream))) return GEMM_ERR_LAUNCH;
+  if (pp.pack_b && !ok(b_kn ? repack_rows(ws + pp.off_b, B, K, N, sms, stream)
+                            : repack_rows(ws + pp.off_b, B, N, K, sms, stream)))
+    return GEMM_ERR_LAUNCH;
+  // Where C is read it ends up aligned with row stride ldc: in the padded D
+  // (which the GEMM then updates in place), in D itself, or as given.
+  void* d_eff = pp.pad_d ? static_cast<void*>(ws + pp.off_d) : D;
+  const void* c_eff = C;
+  if (beta != 0.0f && (pp.pad_d || pp.c_to_d)) {
+    if (!ok(repack_rows(d_eff, C, M, N, sms, stream))) return GEMM_ERR_LAUNCH;
+    c_eff = d_eff;
+  }
+  const uint64_t m = M, n = N, k = K, kp = pp.Kp, np = pp.Np;
+  // With K padded, A's pad columns are +0 and the kernel iterates Kp; an
+  // unpacked B (K x N) simply ends at row K and reads zeros past it.
+  const View a = pp.pack_a ? View{ws + pp.off_a, kp, m, kp} : View{A, k, m, k};
+  View b;
+  if (b_kn)
+    b = pp.pack_b ? View{ws + pp.off_b, np, k, np} : View{B, n, k, n};
+  else
+    b = pp.pack_b ? View{ws + pp.off_b, kp, n, kp} : View{B, k, n, k};
+  const View d = pp.pad_d ? View{d_eff, np, m, np} : View{D, n, m, n};
+  const Scaled sc{c_eff, alpha, beta, b_kn};
+  rc = launch_gemm(M, N, pp.Kp, a, b, d, b_kn, &sc, pp.pad_d ? pp.Np : N, opt, st, stream);
+  if (rc != GEMM_OK) return rc;
+  if (pp.pad_d && !ok(unpack_rows(D, d_eff, M, N, sms, stream))) return GEMM_ERR_LAUNCH;
+  return GEMM_OK;
+}
+
 }  // namespace
 }  // namespace gb300
 
@@ -458,6 +621,24 @@ extern "C" int gemm_f16_scaled(void* D, const void* C, const void* A, const void
                                const gemm_options_t* opt, void* stream) {
   const Scaled sc{C, alpha, beta, b_layout};
   return run(D, A, B, M, N, K, opt, static_cast<cudaStream_t>(stream), &sc);
+}
+
+extern "C" int gemm_padded_workspace_bytes(const void* D, const void* C, const void* A,
+                                           const void* B, int64_t M, int64_t N, int64_t K,
+                                           float beta, int b_layout, uint64_t* bytes) {
+  if (!bytes || M < 0 || N < 0 || K < 0 || M > INT_MAX || N > INT_MAX || K > INT_MAX ||
+      (b_layout != 0 && b_layout != 1))
+    return GEMM_ERR_INVALID_VALUE;
+  *bytes = plan_padding(D, C, A, B, M, N, K, beta, b_layout).total;
+  return GEMM_OK;
+}
+
+extern "C" int gemm_f16_padded(void* D, const void* C, const void* A, const void* B, int64_t M,
+                               int64_t N, int64_t K, float alpha, float beta, int b_layout,
+                               void* workspace, uint64_t workspace_bytes,
+                               const gemm_options_t* opt, void* stream) {
+  return run_padded(D, C, A, B, M, N, K, alpha, beta, b_layout, workspace, workspace_bytes, opt,
+                    static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int gemm_tn_f16_ex(void* D, const void* A, const void* B, int64_t M, int64_t N,

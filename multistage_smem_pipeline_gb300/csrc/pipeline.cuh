@@ -45,8 +45,9 @@ struct GemmParams {
   int32_t b_kn;          // 1: B is K x N row-major (N contiguous): an MN-major operand
   int32_t scaled;        // 1: D = alpha * acc + beta * C instead of D = acc
   float alpha, beta;
-  const uint16_t* C;     // M x N fp16, row stride N; read only when scaled and beta != 0
+  const uint16_t* C;     // M x N fp16, row stride ldc; read only when scaled and beta != 0
   int32_t acc_f16;       // 1: fp16 accumulator (low 16 bits of each TMEM column)
+  int64_t ldc;           // elements between rows of C (a multiple of 8)
 };
 
 // MN-major B: one 64-element N chunk per TMA box; chunks 8 KiB apart.
@@ -120,14 +121,15 @@ __device__ __forceinline__ void widen_f16_accumulator(uint32_t (&r)[32]) {
 }
 
 // r (fp32 bits of one row's 32 accumulator columns) <- alpha * r + beta * C
-// for row `row`, columns [col, col + 32) of C.  Groups of 8 columns past N,
-// and rows past M, are not read (N is a multiple of 8).
+// for row `row`, columns [col, col + 32) of C.  Groups of 8 columns that
+// start at or past N, and rows past M, are not read; a group that straddles N
+// reads up to the next multiple of 8, which the row stride ldc covers.
 __device__ __forceinline__ void apply_alpha_beta(uint32_t (&r)[32], const GemmParams& p, int row,
                                                  int col) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(p.alpha * __uint_as_float(r[i]));
   if (p.beta == 0.0f || row >= p.M) return;
-  const uint16_t* c_row = p.C + static_cast<size_t>(row) * p.N + col;
+  const uint16_t* c_row = p.C + static_cast<size_t>(row) * p.ldc + col;
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
     if (col + 8 * g < p.N) {

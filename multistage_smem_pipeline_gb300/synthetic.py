@@ -29,6 +29,10 @@ c7     8192 x 8192 x 8192       U[-1, 1]; the scaled NN form of "CUDA ç®—å­ç¬”è
 c8     81920 x 256 x 256        U[-1, 1] with an fp16 accumulator: the shape
                                 and the accumulator of the page's own
                                 measurement ("cute(9)", section 11)
+c9     8191 x 8191 x 8191       U[-1, 1]; K and N not multiples of 8, so the
+                                rows are not 16-byte aligned: the general
+                                shapes the padding wrapper of "CUDA ç®—å­ç¬”è®°
+                                2" (GEMM section) serves
 =====  =======================  ===========================================
 """
 from __future__ import annotations
@@ -104,6 +108,7 @@ WORKLOADS = {
     "c6": dict(M=81920, N=256, K=256, kind="uniform"),
     "c7": dict(M=8192, N=8192, K=8192, kind="uniform", b_kn=True, alpha=1.5, beta=-0.5),
     "c8": dict(M=81920, N=256, K=256, kind="uniform", acc_f16=True),
+    "c9": dict(M=8191, N=8191, K=8191, kind="uniform", padded=True),
 }
 WORKLOAD_NAMES = {
     "c1": "gemm_tn_f16 256x256x256 U[-1,1]",
@@ -114,11 +119,12 @@ WORKLOAD_NAMES = {
     "c6": "gemm_tn_f16 tall M=81920 N=256 K=256 U[-1,1]",
     "c7": "gemm_f16_scaled NN 8192x8192x8192 D=1.5*A*B-0.5*C U[-1,1]",
     "c8": "gemm_tn_f16 tall M=81920 N=256 K=256 U[-1,1], fp16 accumulator",
+    "c9": "gemm_f16_padded 8191x8191x8191 U[-1,1] (rows not 16-byte aligned)",
 }
 
 
 def seeds(tag: str) -> tuple[int, int, int]:
-    """(seed_A, seed_B, seed_samples) for a workload tag c1..c8."""
+    """(seed_A, seed_B, seed_samples) for a workload tag c1..c9."""
     c = int(tag[1:])
     return 1000 + c, 2000 + c, 3000 + c
 
@@ -138,7 +144,7 @@ def make_operands(kind: str, M: int, N: int, K: int, seed_a: int, seed_b: int):
 
 
 def workload(tag: str):
-    """(A_bits, B_bits, spec) for a workload tag c1..c8.  B is N x K, or K x N
+    """(A_bits, B_bits, spec) for a workload tag c1..c9.  B is N x K, or K x N
     where spec["b_kn"] is set."""
     spec = WORKLOADS[tag]
     sa, sb, _ = seeds(tag)

@@ -31,7 +31,8 @@ def _declared_functions():
 
 def test_header_declares_the_boundary():
     names = _declared_functions()
-    for want in ("gemm_tn_f16", "gemm_tn_f16_ex", "gemm_f16_scaled", "gemm_get_device_error",
+    for want in ("gemm_tn_f16", "gemm_tn_f16_ex", "gemm_f16_scaled", "gemm_f16_padded",
+                 "gemm_padded_workspace_bytes", "gemm_get_device_error",
                  "gemm_minimum_stages",
                  "gemm_query_config", "gemm_probe_latencies", "gemm_status_string"):
         assert want in names
@@ -172,3 +173,77 @@ def test_status_strings(binding):
     assert binding.status_string(0) == "GEMM_OK"
     assert binding.status_string(5) == "GEMM_ERR_TIMEOUT"
     assert binding.status_string(99) == "GEMM_ERR_UNKNOWN"
+
+
+def _ws_bytes(binding, D, C, A, B, M, N, K, beta=0.0, layout=0):
+    n = ctypes.c_uint64(12345)
+    rc = binding.LIB.gemm_padded_workspace_bytes(D, C, A, B, M, N, K, beta, layout, ctypes.byref(n))
+    return rc, n.value
+
+
+def test_padded_workspace_sizes(binding):
+    # nothing misaligned: no workspace
+    assert _ws_bytes(binding, P0, P1, P1 + 4096, P2, 10, 16, 16, beta=1.0) == (0, 0)
+    # K = 15: A (10 x 16) and an N x K B (16 x 16) repacked, 256-byte regions
+    assert _ws_bytes(binding, P0, 0, P1, P2, 10, 16, 15) == (0, 512 + 512)
+    # N = 13 with a K x N B: B (16 x 16) and D (10 x 16) padded; A as given
+    assert _ws_bytes(binding, P0, 0, P1, P2, 10, 13, 16, layout=1) == (0, 512 + 512)
+    # ... while an N x K B (13 x 16) is aligned as it is
+    assert _ws_bytes(binding, P0, 0, P1, P2, 10, 13, 16, layout=0) == (0, 512)
+    # a base address alone forces a repack of that operand
+    assert _ws_bytes(binding, P0 + 2, 0, P1, P2, 10, 16, 16) == (0, 512)
+    assert _ws_bytes(binding, P0, 0, P1 + 6, P2, 10, 16, 16) == (0, 512)
+    assert _ws_bytes(binding, P0, 0, P1, P2 + 4, 300, 16, 16) == (0, 512)
+    # a misaligned C with an aligned D is copied into D: no region of its own
+    assert _ws_bytes(binding, P0, P1 + 2, P2, P2 + 65536, 10, 16, 16, beta=0.5) == (0, 0)
+    # nothing reaches the GEMM kernel: no workspace
+    assert _ws_bytes(binding, P0 + 2, 0, P1 + 2, P2 + 2, 10, 13, 0) == (0, 0)
+    assert _ws_bytes(binding, P0 + 2, 0, P1 + 2, P2 + 2, 0, 13, 7) == (0, 0)
+    # large sizes: 8191^3 repacks A, B and D, each 8191 x 8192 fp16
+    region = (8191 * 8192 * 2 + 255) // 256 * 256
+    assert _ws_bytes(binding, P0, 0, P1, P2, 8191, 8191, 8191) == (0, 3 * region)
+    E = binding.GEMM_ERR_INVALID_VALUE
+    assert _ws_bytes(binding, P0, 0, P1, P2, -1, 16, 16)[0] == E
+    assert _ws_bytes(binding, P0, 0, P1, P2, 16, 16, 16, layout=2)[0] == E
+    assert binding.LIB.gemm_padded_workspace_bytes(P0, 0, P1, P2, 1, 1, 1, 0.0, 0, None) == E
+
+
+def _padded(binding, D, C, A, B, M, N, K, ws=0, ws_bytes=0, alpha=1.0, beta=0.0, layout=0):
+    o = binding._options()
+    return binding.LIB.gemm_f16_padded(D, C, A, B, M, N, K, alpha, beta, layout, ws, ws_bytes,
+                                       ctypes.byref(o), None)
+
+
+def test_padded_entry_rejects_bad_arguments(binding):
+    E, MIS = binding.GEMM_ERR_INVALID_VALUE, binding.GEMM_ERR_MISALIGNED
+    W = 0x40000000
+    # odd (not fp16-aligned) pointers
+    assert _padded(binding, P0 + 1, 0, P1, P2, 16, 16, 16) == MIS
+    assert _padded(binding, P0, 0, P1 + 3, P2, 16, 16, 16) == MIS
+    assert _padded(binding, P0, P1 + 8192 + 1, P2, P2 + 65536, 16, 16, 16, beta=1.0) == MIS
+    # workspace missing, too small, misaligned, or overlapping an operand
+    need = _ws_bytes(binding, P0, 0, P1, P2, 16, 13, 15)[1]
+    assert need > 0
+    assert _padded(binding, P0, 0, P1, P2, 16, 13, 15) == E
+    assert _padded(binding, P0, 0, P1, P2, 16, 13, 15, ws=W, ws_bytes=need - 1) == E
+    assert _padded(binding, P0, 0, P1, P2, 16, 13, 15, ws=W + 8, ws_bytes=need) == MIS
+    assert _padded(binding, P0, 0, P1, P2, 16, 13, 15, ws=P0 - 64, ws_bytes=need) == E
+    assert _padded(binding, P0, 0, P1, P2, 16, 13, 15, ws=P1 + 64, ws_bytes=need) == E
+    # the checks of the scaled form
+    assert _padded(binding, P0, 0, P1, P2, 16, 13, 15, ws=W, ws_bytes=need, layout=2) == E
+    assert _padded(binding, P0, 0, P1, P2, 16, 13, 15, ws=W, ws_bytes=need,
+                   alpha=float("nan")) == E
+    assert _padded(binding, P0, 0, P1, P2, 16, 13, 15, ws=W, ws_bytes=need, beta=1.0) == E
+    assert _padded(binding, P0, P0 + 2, P1, P2, 16, 13, 15, ws=W, ws_bytes=need, beta=1.0) == E
+    assert _padded(binding, P0, 0, P0 + 64, P2, 16, 13, 15, ws=W, ws_bytes=need) == E
+    assert _padded(binding, P0, 0, P1, P2, -3, 13, 15) == E
+    # empty outputs are no-ops without a workspace or a device
+    assert _padded(binding, 0, 0, 0, 0, 0, 13, 15) == binding.GEMM_OK
+    assert _padded(binding, P0 + 2, 0, 0, 0, 7, 0, 15) == binding.GEMM_OK
+
+
+@pytest.mark.skipif(cuda_available(), reason="checks the no-device error path")
+def test_padded_call_without_a_device_reports_cuda_error(binding):
+    need = _ws_bytes(binding, P0, 0, P1, P2, 16, 13, 15)[1]
+    assert _padded(binding, P0, 0, P1, P2, 16, 13, 15, ws=0x40000000, ws_bytes=need) in \
+        (binding.GEMM_ERR_CUDA, binding.GEMM_ERR_UNSUPPORTED_DEVICE)

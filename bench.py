@@ -336,7 +336,7 @@ def run_gpu(args, tag):
     stream = torch.cuda.current_stream(dev)
     opts = {"path": ["auto", "square", "skinny", "pair"].index(args.path), "bn": args.bn,
             "kstage": args.kstage, "katoms": args.katoms, "group_m": args.group_m,
-            "epi_warps": args.epi_warps}
+            "epi_warps": args.epi_warps, "b_resident": args.b_resident}
     forced = any(opts.values())
     cfg = binding.query_config(M, N, K, b_layout=1 if spec.get("b_kn") else 0, **opts)
 
@@ -565,6 +565,7 @@ def run_gpu(args, tag):
                 "path": ["auto", "square", "skinny", "pair"][cfg["path"]], "bm": cfg["bm"],
                 "bn": cfg["bn"], "bk": cfg["bk"], "kstage": cfg["kstage"], "ctas": cfg["ctas"],
                 "tiles": cfg["tiles"], "katoms": cfg["katoms"], "epi_warps": cfg["epi_warps"],
+                "b_resident": cfg["b_resident"],
                 "forced": forced}),
             "launch_ms": ({"mean": ms, "median": statistics.median(launches_ms),
                            "p10": float(np.percentile(launches_ms, 10)),
@@ -618,6 +619,8 @@ def main():
                     help="diagnostics: force a kernel path (default: the library's choice)")
     ap.add_argument("--bn", type=int, default=0, help="diagnostics: force the tile width")
     ap.add_argument("--kstage", type=int, default=0, help="diagnostics: force the ring depth")
+    ap.add_argument("--b-resident", type=int, default=0, choices=[0, 1, 2],
+                    help="diagnostics: resident B (0 choose, 1 never, 2 always)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

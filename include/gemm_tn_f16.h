@@ -89,6 +89,10 @@ typedef struct {
   int acc_f16;         /* 0: fp32 accumulator (default); 1: fp16 accumulator, rounded
                           after every 16-deep K slice -- the arithmetic of the
                           F16F16F16F16 MMA atom of "cute(9) multistage_gemm" */
+  int b_resident;      /* 0 = choose; 1 = never; 2 = always (else GEMM_ERR_INVALID_VALUE).
+                          Resident B: on a single-CTA path with one n-block (N <= bn)
+                          and an N x K B, each CTA loads all of B into shared memory
+                          once and its ring streams only A (the tall shapes) */
 } gemm_options_t;
 
 /* gemm_tn_f16 with an explicit configuration (sweeps, tests).  Same
@@ -179,6 +183,7 @@ typedef struct {
   int smem_bytes, tmem_cols;
   int katoms;          /* bk = 64 * katoms */
   int epi_warps;       /* threads per CTA = 64 + 32 * epi_warps */
+  int b_resident;      /* 1: B is held in shared memory for the whole kernel */
 } gemm_config_t;
 int gemm_query_config(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt,
                       gemm_config_t* out);

@@ -10,6 +10,9 @@
 //                          thread already fills the second TMEM accumulator;
 //                          with 8 warps two share each TMEM lane quadrant and
 //                          take alternate 32-column chunks.
+// With one n-block (N <= BN) every tile multiplies by the same B; in the
+// resident-B mode the producer loads all of B (BN x K) once into its own
+// shared-memory region and the ring carries only A slices.
 //
 // This is the multistage pipeline of "cute(9) multistage_gemm" (sections 4-6:
 // a ring of kStage K-tiles, a prologue that runs ahead, a mainloop that
@@ -72,7 +75,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
   uint8_t* const smem = smem_raw + (base - raw);
   constexpr int kThreads = threads_for(kEpiWarps);
   constexpr int kChunkStride = kEpiWarps / 4;  // warps sharing a TMEM lane quadrant
-  const SmemLayout L = SmemLayout::make(p.stages, p.stage_bytes, kEpiWarps);
+  const SmemLayout L = SmemLayout::make(p.stages, p.stage_bytes, kEpiWarps, p.bres_bytes);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -83,6 +86,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
   auto tfull_bar = [&](int b) { return bars + 8u * (2 * S + b); };
   auto tempty_bar = [&](int b) { return bars + 8u * (2 * S + 2 + b); };
   const uint32_t drain_bar = bars + 8u * (2 * S + 4);
+  const uint32_t bres_bar = bars + 8u * (2 * S + 5);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc + 4);
 
@@ -96,6 +100,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
       mbar_init(tempty_bar(b), kEpiWarps); // one arrive per epilogue warp
     }
     mbar_init(drain_bar, 1);
+    mbar_init(bres_bar, 1);  // producer's arrive.expect_tx for the resident B
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -128,6 +133,14 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0;
+      if (p.b_resident) {
+        // One n-block: every tile multiplies by the same B.  Load all of its
+        // 64-wide K slices once, behind one barrier; the ring carries A only.
+        const int slices = p.num_k_blocks * p.katoms;
+        mbar_arrive_expect_tx(bres_bar, p.bres_bytes);
+        for (int j = 0; j < slices; ++j)
+          tma_load_2d(base + L.bres + j * p.b_atom_bytes, &tmB, bres_bar, j * kBK, 0);
+      }
       for (int t = blockIdx.x; t < p.num_tiles && !*abort_flag; t += gridDim.x) {
         int mb, nb;
         tile_coords(t, p, mb, nb);
@@ -150,7 +163,9 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
                 tma_load_2d_hint(ad, &tmA, full_bar(stage), x, mb * kBM, pol_a);
               else
                 tma_load_2d(ad, &tmA, full_bar(stage), x, mb * kBM);
-              if (p.b_kn) {  // B is K x N: one 64-column box per chunk of the tile
+              if (p.b_resident) {
+                // B is already in its own region
+              } else if (p.b_kn) {  // B is K x N: one 64-column box per chunk of the tile
                 for (int ch = 0; ch < p.bn / 64; ++ch)
                   tma_load_2d(bd + ch * kMnChunkBytes, &tmB, full_bar(stage), nb * p.bn + 64 * ch,
                               x);
@@ -174,6 +189,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
       const uint32_t first = issued > static_cast<uint32_t>(S) ? issued - S : 0u;
       for (uint32_t i = first; i < issued; ++i)
         wait_timed(full_bar(i % S), (i / S) & 1u, p.timeout_ns);
+      if (p.b_resident) wait_timed(bres_bar, 0, p.timeout_ns);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -183,21 +199,33 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
+      bool b_ready = !p.b_resident;
       for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
         if (!wait_or_abort(tempty_bar(acc), acc_phase ^ 1u, p.timeout_ns, abort_flag,
                            kSiteTmemEmpty))
           break;
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * p.bn);
+        const int k0 = first_k_block(t, p);
         bool ok = true;
         for (int i = 0; i < p.num_k_blocks; ++i) {
           if (!wait_or_abort(full_bar(stage), phase, p.timeout_ns, abort_flag, kSiteFull)) {
             ok = false;
             break;
           }
+          if (!b_ready) {  // the resident B, once
+            if (!wait_or_abort(bres_bar, 0, p.timeout_ns, abort_flag, kSiteFull)) {
+              ok = false;
+              break;
+            }
+            b_ready = true;
+          }
           tc_fence_after_sync();
           const uint32_t a_src = base + L.ring + stage * p.stage_bytes;
-          const uint32_t b_src = a_src + p.katoms * kABytes;
+          const int kb = (k0 + i < p.num_k_blocks) ? k0 + i : k0 + i - p.num_k_blocks;
+          const uint32_t b_src = p.b_resident
+                                     ? base + L.bres + kb * p.katoms * p.b_atom_bytes
+                                     : a_src + p.katoms * kABytes;
           for (int at = 0; at < p.katoms; ++at) {
             const uint64_t a_desc = sw128_kmajor_desc(a_src + at * kABytes);
             const uint64_t b_desc =

@@ -92,14 +92,16 @@ uint32_t make_idesc(int m, int n) {
   return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 
-int stages_that_fit(uint32_t stage_bytes, int epi_warps) {
-  const uint32_t fixed = epi_warps * kEpiBufs * kEpiChunkBytes + 16 + 1024;
+// Deepest ring (at least 2) whose carve-up, plus 1 KiB of alignment slack,
+// fits the dynamic shared memory limit; 1 if not even 2 stages fit.
+int stages_that_fit(uint32_t stage_bytes, int epi_warps, uint32_t bres_bytes = 0) {
+  const auto fits = [&](int s) {
+    return SmemLayout::make(s, stage_bytes, epi_warps, bres_bytes).total + 1024 <=
+           static_cast<uint32_t>(kMaxDynSmem);
+  };
+  if (!fits(2)) return 1;
   int s = 2;
-  while (s + 1 <= kMaxStages) {
-    const uint32_t bars = 8u * (2 * (s + 1) + 5);
-    if ((s + 1) * stage_bytes + fixed + bars > static_cast<uint32_t>(kMaxDynSmem)) break;
-    ++s;
-  }
+  while (s + 1 <= kMaxStages && fits(s + 1)) ++s;
   return s;
 }
 
@@ -133,6 +135,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   if (o.path < 0 || o.path > 3 || o.bn < 0 || o.bn > 256 || (o.bn % 32) != 0 || o.kstage < 0 ||
       o.kstage == 1 || o.kstage > kMaxStages || o.max_ctas < 0 || o.group_m < 0 || o.inject < 0 ||
       o.inject > 1 || o.katoms < 0 || o.katoms > 2 || o.acc_f16 < 0 || o.acc_f16 > 1 ||
+      o.b_resident < 0 || o.b_resident > 2 ||
       (o.epi_warps != 0 && o.epi_warps != 4 && o.epi_warps != 8))
     return GEMM_ERR_INVALID_VALUE;
   if (o.path == GEMM_PATH_SKINNY && M > kBM) return GEMM_ERR_INVALID_VALUE;
@@ -158,6 +161,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
     }
     for (int cand = 256; cand >= 32; cand -= 32) {
       if (o.bn && cand != o.bn) continue;
+      if (o.b_resident == 2 && cand < N) continue;  // resident B needs a single n-block
       // a K x N B is loaded in 64-column boxes: each CTA's share of BN must be whole boxes
       if (b_kn && cand % (kind == GEMM_PATH_PAIR ? 128 : 64) != 0) continue;
       const int bm = (kind == GEMM_PATH_PAIR) ? 2 * kBM : kBM;
@@ -185,16 +189,45 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   // loop per tile is short (the epilogue is then the critical path), four
   // are enough -- and leave the MMA and producer warps their issue slots --
   // when it is long.
-  const int epi_warps = o.epi_warps ? o.epi_warps : (K <= 1024 ? 8 : 4);
+  int epi_warps = o.epi_warps ? o.epi_warps : (K <= 1024 ? 8 : 4);
   // Two 64-wide K slices per stage halve the issuing threads' per-byte
   // barrier/commit work (measured: +12 % at 8192^3); used whenever the ring
   // still gets at least 3 stages.
-  const int katoms =
-      o.katoms ? o.katoms
-               : (stages_that_fit(stage_bytes_for(path, bn, 2), epi_warps) >= 3 ? 2 : 1);
+  int katoms = o.katoms ? o.katoms
+                        : (stages_that_fit(stage_bytes_for(path, bn, 2), epi_warps) >= 3 ? 2 : 1);
+  // Resident B: with one n-block every tile multiplies by the same B, so a
+  // single-CTA kernel can hold all of it in shared memory and stream only A
+  // -- a third of the bytes per 128 x 256 tile when K = N = 256.  Used when
+  // each CTA has at least two tiles and the ring still gets 3 stages of A.
+  bool b_resident = false;
+  uint32_t bres_bytes = 0;
+  const bool res_possible = path != GEMM_PATH_PAIR && num_n == 1 && !b_kn;
+  if (o.b_resident == 2 && !res_possible) return GEMM_ERR_INVALID_VALUE;
+  if (res_possible && (o.b_resident == 2 || (o.b_resident == 0 && tiles >= 2 * sms))) {
+    const int min_stages = (o.b_resident == 2) ? 2 : 3;
+    for (int ew : {epi_warps, 4}) {
+      if (b_resident || (o.epi_warps && ew != o.epi_warps)) continue;
+      for (int ka : {2, 1}) {
+        if (b_resident || (o.katoms && ka != o.katoms)) continue;
+        const uint32_t bres = static_cast<uint32_t>((K + kBK * ka - 1) / (kBK * ka)) * ka *
+                              b_atom_bytes_for(path, bn);
+        if (bres > static_cast<uint32_t>(kMaxDynSmem)) continue;
+        const int f = stages_that_fit(static_cast<uint32_t>(ka) * kABytes, ew, bres);
+        if (f >= min_stages && (ka == 1 || o.katoms || f >= 3)) {
+          b_resident = true;
+          bres_bytes = bres;
+          epi_warps = ew;
+          katoms = ka;
+        }
+      }
+    }
+    if (o.b_resident == 2 && !b_resident) return GEMM_ERR_INVALID_VALUE;
+  }
   const int64_t num_k = (K + kBK * katoms - 1) / (kBK * katoms);
-  const uint32_t stage_bytes = stage_bytes_for(path, bn, katoms);
-  const int fit = stages_that_fit(stage_bytes, epi_warps);
+  const uint32_t stage_bytes = b_resident ? static_cast<uint32_t>(katoms) * kABytes
+                                          : stage_bytes_for(path, bn, katoms);
+  const int fit = stages_that_fit(stage_bytes, epi_warps, bres_bytes);
+  if (fit < 2) return GEMM_ERR_INVALID_VALUE;
   const int stages = o.kstage ? o.kstage : fit;
   if (stages > fit) return GEMM_ERR_INVALID_VALUE;
   int ctas;
@@ -207,7 +240,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
     if (o.max_ctas) ctas = std::min(ctas, o.max_ctas);
   }
   const int group_m = o.group_m ? o.group_m : (path == GEMM_PATH_PAIR ? 8 : 16);
-  const SmemLayout L = SmemLayout::make(stages, stage_bytes, epi_warps);
+  const SmemLayout L = SmemLayout::make(stages, stage_bytes, epi_warps, bres_bytes);
 
   Plan pl;
   std::memset(&pl, 0, sizeof(pl));
@@ -223,6 +256,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   pl.cfg.tiles = static_cast<int>(tiles);
   pl.cfg.smem_bytes = static_cast<int>(L.total + 1024);  // + alignment slack
   pl.cfg.tmem_cols = static_cast<int>(pow2_at_least(2u * bn));
+  pl.cfg.b_resident = b_resident ? 1 : 0;
 
   GemmParams& p = pl.p;
   p.M = static_cast<int32_t>(M);
@@ -244,6 +278,8 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   p.b_atom_bytes = b_atom_bytes_for(path, bn);
   p.katoms = katoms;
   p.epi_warps = epi_warps;
+  p.b_resident = b_resident ? 1 : 0;
+  p.bres_bytes = bres_bytes;
   // One m-block: every tile reads the same rows of A (keep them in L2, stream
   // B through it once) and the k loops are rotated across tiles.
   p.l2_hints = (num_m == 1) ? 3u : 0u;

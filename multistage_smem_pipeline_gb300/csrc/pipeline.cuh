@@ -48,6 +48,9 @@ struct GemmParams {
   const uint16_t* C;     // M x N fp16, row stride ldc; read only when scaled and beta != 0
   int32_t acc_f16;       // 1: fp16 accumulator (low 16 bits of each TMEM column)
   int64_t ldc;           // elements between rows of C (a multiple of 8)
+  int32_t b_resident;    // 1: all of B (one n-block, every k slice) is loaded once per CTA
+                         //    into its own region; the ring then carries A only
+  uint32_t bres_bytes;   // size of that region: num_k_blocks * katoms * b_atom_bytes (else 0)
 };
 
 // MN-major B: one 64-element N chunk per TMA box; chunks 8 KiB apart.
@@ -63,15 +66,20 @@ __device__ __forceinline__ int first_k_block(int t, const GemmParams& p) {
          p.num_k_blocks;
 }
 
-// Shared-memory carve-up, offsets from the 1024-aligned base.
+// Shared-memory carve-up, offsets from the 1024-aligned base: the ring, the
+// resident B region (if any; 1024-aligned since stages are whole 16 KiB A
+// slices), the epilogue staging buffers, then 2 * stages + 6 mbarriers
+// (full, empty, 2 tmem-full, 2 tmem-empty, drain, resident-B full).
 struct SmemLayout {
-  uint32_t ring, epi, bars, misc, total;
-  __host__ __device__ static SmemLayout make(int stages, uint32_t stage_bytes, int epi_warps) {
+  uint32_t ring, bres, epi, bars, misc, total;
+  __host__ __device__ static SmemLayout make(int stages, uint32_t stage_bytes, int epi_warps,
+                                             uint32_t bres_bytes = 0) {
     SmemLayout L;
     L.ring = 0;
-    L.epi = stages * stage_bytes;
+    L.bres = stages * stage_bytes;
+    L.epi = L.bres + bres_bytes;
     L.bars = L.epi + epi_warps * kEpiBufs * kEpiChunkBytes;
-    L.misc = L.bars + 8 * (2 * stages + 5);
+    L.misc = L.bars + 8 * (2 * stages + 6);
     L.total = L.misc + 16;
     return L;
   }

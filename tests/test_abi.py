@@ -101,7 +101,8 @@ def test_rejects_bad_options(binding):
     for kw in [dict(bn=48), dict(bn=512), dict(kstage=1), dict(kstage=17), dict(path=4),
                dict(inject=2), dict(max_ctas=-1), dict(path=binding.PATH_SKINNY),
                dict(katoms=3), dict(katoms=-1), dict(epi_warps=6), dict(epi_warps=16),
-               dict(acc_f16=2)]:
+               dict(acc_f16=2), dict(b_resident=3), dict(b_resident=-1),
+               dict(b_resident=2, path=binding.PATH_PAIR), dict(b_resident=2, bn=32)]:
         o = binding._options(**kw)
         M = 256 if kw.get("path") == binding.PATH_SKINNY else 64
         assert _call(binding, P0, P1, P2, M, 64, 64, o) == binding.GEMM_ERR_INVALID_VALUE, kw
@@ -247,3 +248,22 @@ def test_padded_call_without_a_device_reports_cuda_error(binding):
     need = _ws_bytes(binding, P0, 0, P1, P2, 16, 13, 15)[1]
     assert _padded(binding, P0, 0, P1, P2, 16, 13, 15, ws=0x40000000, ws_bytes=need) in \
         (binding.GEMM_ERR_CUDA, binding.GEMM_ERR_UNSUPPORTED_DEVICE)
+
+
+def test_resident_b_plans(binding):
+    # the tall shape the multistage page times: one n-block, 640 tiles, so each
+    # CTA holds all of B (256 x 256 fp16) and streams only A
+    cfg = binding.query_config(81920, 256, 256)
+    assert cfg["b_resident"] == 1 and cfg["path"] == binding.PATH_SQUARE
+    assert cfg["smem_bytes"] <= 232448
+    # off on request, and never for several n-blocks, the pair path or a K x N B
+    assert binding.query_config(81920, 256, 256, b_resident=1)["b_resident"] == 0
+    assert binding.query_config(8192, 8192, 8192)["b_resident"] == 0
+    assert binding.query_config(81920, 512, 256)["b_resident"] == 0
+    assert binding.query_config(81920, 256, 256, b_layout=1)["b_resident"] == 0
+    # too few tiles per CTA to pay for loading B up front
+    assert binding.query_config(1024, 256, 256)["b_resident"] == 0
+    # forced: the tile is widened to cover N; a B too large for shared memory is refused
+    assert binding.query_config(300, 256, 256, path=1, b_resident=2)["bn"] == 256
+    with pytest.raises(binding.GemmError):
+        binding.query_config(4096, 256, 4096, path=1, b_resident=2)

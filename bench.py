@@ -336,7 +336,7 @@ def run_gpu(args, tag):
     stream = torch.cuda.current_stream(dev)
     opts = {"path": ["auto", "square", "skinny", "pair"].index(args.path), "bn": args.bn,
             "kstage": args.kstage, "katoms": args.katoms, "group_m": args.group_m,
-            "epi_warps": args.epi_warps, "b_resident": args.b_resident}
+            "epi_warps": args.epi_warps, "b_resident": args.b_resident, "pdl": args.pdl}
     forced = any(opts.values())
     cfg = binding.query_config(M, N, K, b_layout=1 if spec.get("b_kn") else 0, **opts)
 
@@ -536,8 +536,9 @@ def run_gpu(args, tag):
         if iso:
             iso["tflops_clean_flush"] = flops / (iso["mean_ms_clean_flush"] * 1e-3) / 1e12
             iso["frac_of_burst_peak"] = iso["tflops_clean_flush"] / float(peaks["bf16_tflops"])
-    roof["kernel"] = "gemm_tn_f16_%s<%d>" % ("pair" if cfg["path"] == 3 else "persistent",
-                                             cfg["epi_warps"])
+    roof["kernel"] = ("gemm_tn_f16_pair<%d>" % cfg["epi_warps"] if cfg["path"] == 3 else
+                      "gemm_tn_f16_persistent<%d, %s>" % (cfg["epi_warps"],
+                                                          "true" if cfg["b_resident"] else "false"))
     if kernel_ms is not None:
         roof["kernel_ms"] = kernel_ms
         roof["kernel_timing"] = kernel_note
@@ -565,7 +566,7 @@ def run_gpu(args, tag):
                 "path": ["auto", "square", "skinny", "pair"][cfg["path"]], "bm": cfg["bm"],
                 "bn": cfg["bn"], "bk": cfg["bk"], "kstage": cfg["kstage"], "ctas": cfg["ctas"],
                 "tiles": cfg["tiles"], "katoms": cfg["katoms"], "epi_warps": cfg["epi_warps"],
-                "b_resident": cfg["b_resident"],
+                "b_resident": cfg["b_resident"], "pdl": cfg["pdl"],
                 "forced": forced}),
             "launch_ms": ({"mean": ms, "median": statistics.median(launches_ms),
                            "p10": float(np.percentile(launches_ms, 10)),
@@ -621,6 +622,8 @@ def main():
     ap.add_argument("--kstage", type=int, default=0, help="diagnostics: force the ring depth")
     ap.add_argument("--b-resident", type=int, default=0, choices=[0, 1, 2],
                     help="diagnostics: resident B (0 choose, 1 never, 2 always)")
+    ap.add_argument("--pdl", type=int, default=0, choices=[0, 1],
+                    help="diagnostics: 1 = launch without programmatic dependent launch")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

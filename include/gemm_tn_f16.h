@@ -93,6 +93,10 @@ typedef struct {
                           Resident B: on a single-CTA path with one n-block (N <= bn)
                           and an N x K B, each CTA loads all of B into shared memory
                           once and its ring streams only A (the tall shapes) */
+  int pdl;             /* 0: launch with programmatic stream serialization (the
+                          kernel's set-up overlaps the end of the previous kernel
+                          in the stream; it waits for that kernel -- griddepcontrol
+                          -- before touching global memory); 1: plain launch */
 } gemm_options_t;
 
 /* gemm_tn_f16 with an explicit configuration (sweeps, tests).  Same
@@ -184,6 +188,7 @@ typedef struct {
   int katoms;          /* bk = 64 * katoms */
   int epi_warps;       /* threads per CTA = 64 + 32 * epi_warps */
   int b_resident;      /* 1: B is held in shared memory for the whole kernel */
+  int pdl;             /* 1: launched with programmatic stream serialization */
 } gemm_config_t;
 int gemm_query_config(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt,
                       gemm_config_t* out);

@@ -64,7 +64,9 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uin
   }
 }
 
-template <int kEpiWarps>
+// kResident selects the resident-B mode at compile time (p.b_resident must
+// agree), so the streaming kernel's loops carry none of its code.
+template <int kEpiWarps, bool kResident>
 __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
     gemm_tn_f16_persistent(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
@@ -75,7 +77,8 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
   uint8_t* const smem = smem_raw + (base - raw);
   constexpr int kThreads = threads_for(kEpiWarps);
   constexpr int kChunkStride = kEpiWarps / 4;  // warps sharing a TMEM lane quadrant
-  const SmemLayout L = SmemLayout::make(p.stages, p.stage_bytes, kEpiWarps, p.bres_bytes);
+  const SmemLayout L =
+      SmemLayout::make(p.stages, p.stage_bytes, kEpiWarps, kResident ? p.bres_bytes : 0u);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -91,6 +94,9 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc + 4);
 
   if (threadIdx.x == 0) {
+    // The next GEMM in the stream may start its own set-up on SMs this grid
+    // frees; its griddepcontrol.wait still orders it after this grid.
+    grid_launch_dependents();
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);   // producer's arrive.expect_tx; TMA bytes complete it
       mbar_init(empty_bar(s), 1);  // one tcgen05.commit per consumed stage
@@ -124,6 +130,9 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
     tc_fence_after_sync();
     tmem_base = *tmem_slot;
   }
+  // Set-up done without touching global memory; from here on the previous
+  // kernel's results must be complete and visible.
+  grid_dependency_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -133,7 +142,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0;
-      if (p.b_resident) {
+      if (kResident) {
         // One n-block: every tile multiplies by the same B.  Load all of its
         // 64-wide K slices once, behind one barrier; the ring carries A only.
         const int slices = p.num_k_blocks * p.katoms;
@@ -163,7 +172,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
                 tma_load_2d_hint(ad, &tmA, full_bar(stage), x, mb * kBM, pol_a);
               else
                 tma_load_2d(ad, &tmA, full_bar(stage), x, mb * kBM);
-              if (p.b_resident) {
+              if (kResident) {
                 // B is already in its own region
               } else if (p.b_kn) {  // B is K x N: one 64-column box per chunk of the tile
                 for (int ch = 0; ch < p.bn / 64; ++ch)
@@ -189,7 +198,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
       const uint32_t first = issued > static_cast<uint32_t>(S) ? issued - S : 0u;
       for (uint32_t i = first; i < issued; ++i)
         wait_timed(full_bar(i % S), (i / S) & 1u, p.timeout_ns);
-      if (p.b_resident) wait_timed(bres_bar, 0, p.timeout_ns);
+      if (kResident) wait_timed(bres_bar, 0, p.timeout_ns);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -199,21 +208,21 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      bool b_ready = !p.b_resident;
+      bool b_ready = !kResident;
       for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
         if (!wait_or_abort(tempty_bar(acc), acc_phase ^ 1u, p.timeout_ns, abort_flag,
                            kSiteTmemEmpty))
           break;
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * p.bn);
-        const int k0 = first_k_block(t, p);
+        const int k0 = kResident ? first_k_block(t, p) : 0;
         bool ok = true;
         for (int i = 0; i < p.num_k_blocks; ++i) {
           if (!wait_or_abort(full_bar(stage), phase, p.timeout_ns, abort_flag, kSiteFull)) {
             ok = false;
             break;
           }
-          if (!b_ready) {  // the resident B, once
+          if (kResident && !b_ready) {  // the resident B, once
             if (!wait_or_abort(bres_bar, 0, p.timeout_ns, abort_flag, kSiteFull)) {
               ok = false;
               break;
@@ -222,10 +231,11 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
           }
           tc_fence_after_sync();
           const uint32_t a_src = base + L.ring + stage * p.stage_bytes;
-          const int kb = (k0 + i < p.num_k_blocks) ? k0 + i : k0 + i - p.num_k_blocks;
-          const uint32_t b_src = p.b_resident
-                                     ? base + L.bres + kb * p.katoms * p.b_atom_bytes
-                                     : a_src + p.katoms * kABytes;
+          uint32_t b_src = a_src + p.katoms * kABytes;
+          if (kResident) {
+            const int kb = (k0 + i < p.num_k_blocks) ? k0 + i : k0 + i - p.num_k_blocks;
+            b_src = base + L.bres + kb * p.katoms * p.b_atom_bytes;
+          }
           for (int at = 0; at < p.katoms; ++at) {
             const uint64_t a_desc = sw128_kmajor_desc(a_src + at * kABytes);
             const uint64_t b_desc =

@@ -63,6 +63,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc + 4);
 
   if (threadIdx.x == 0) {
+    grid_launch_dependents();  // see gemm_tn_f16_persistent
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
@@ -92,6 +93,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
   cluster_sync();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  grid_dependency_wait();  // first global-memory access follows
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer (both CTAs)

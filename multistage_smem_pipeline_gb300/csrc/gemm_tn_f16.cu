@@ -135,7 +135,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   if (o.path < 0 || o.path > 3 || o.bn < 0 || o.bn > 256 || (o.bn % 32) != 0 || o.kstage < 0 ||
       o.kstage == 1 || o.kstage > kMaxStages || o.max_ctas < 0 || o.group_m < 0 || o.inject < 0 ||
       o.inject > 1 || o.katoms < 0 || o.katoms > 2 || o.acc_f16 < 0 || o.acc_f16 > 1 ||
-      o.b_resident < 0 || o.b_resident > 2 ||
+      o.b_resident < 0 || o.b_resident > 2 || o.pdl < 0 || o.pdl > 1 ||
       (o.epi_warps != 0 && o.epi_warps != 4 && o.epi_warps != 8))
     return GEMM_ERR_INVALID_VALUE;
   if (o.path == GEMM_PATH_SKINNY && M > kBM) return GEMM_ERR_INVALID_VALUE;
@@ -257,6 +257,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   pl.cfg.smem_bytes = static_cast<int>(L.total + 1024);  // + alignment slack
   pl.cfg.tmem_cols = static_cast<int>(pow2_at_least(2u * bn));
   pl.cfg.b_resident = b_resident ? 1 : 0;
+  pl.cfg.pdl = o.pdl ? 0 : 1;
 
   GemmParams& p = pl.p;
   p.M = static_cast<int32_t>(M);
@@ -317,10 +318,14 @@ int prepare_device(DeviceState* st) {
   std::lock_guard<std::mutex> lk(g_mu);
   if (st->smem_attr == kMaxDynSmem && st->pair_smem_attr == kMaxDynSmem && st->max_pairs > 0)
     return GEMM_OK;
-  if (cudaFuncSetAttribute(gemm_tn_f16_persistent<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kMaxDynSmem) != cudaSuccess ||
-      cudaFuncSetAttribute(gemm_tn_f16_persistent<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kMaxDynSmem) != cudaSuccess ||
+  if (cudaFuncSetAttribute(gemm_tn_f16_persistent<4, false>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem) != cudaSuccess ||
+      cudaFuncSetAttribute(gemm_tn_f16_persistent<8, false>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem) != cudaSuccess ||
+      cudaFuncSetAttribute(gemm_tn_f16_persistent<4, true>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem) != cudaSuccess ||
+      cudaFuncSetAttribute(gemm_tn_f16_persistent<8, true>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem) != cudaSuccess ||
       cudaFuncSetAttribute(gemm_tn_f16_pair<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kMaxDynSmem) != cudaSuccess ||
       cudaFuncSetAttribute(gemm_tn_f16_pair<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -450,35 +455,46 @@ int launch_gemm(int64_t M, int64_t N, int64_t K, const View& a, const View& b, c
       encode_2d(&tmD, d, kEpiCols, 32, CU_TENSOR_MAP_SWIZZLE_64B) != GEMM_OK)
     return GEMM_ERR_INVALID_VALUE;
 
-  const int threads = threads_for(pl.cfg.epi_warps);
-  if (!pair) {
-    if (pl.cfg.epi_warps == 8)
-      gemm_tn_f16_persistent<8><<<pl.cfg.ctas, threads, pl.cfg.smem_bytes, stream>>>(tmA, tmB, tmD,
-                                                                                   pl.p);
-    else
-      gemm_tn_f16_persistent<4><<<pl.cfg.ctas, threads, pl.cfg.smem_bytes, stream>>>(tmA, tmB, tmD,
-                                                                                   pl.p);
-  } else {
-    cudaLaunchConfig_t cfg;
-    std::memset(&cfg, 0, sizeof(cfg));
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(pl.cfg.ctas, 1, 1);
-    cfg.blockDim = dim3(threads, 1, 1);
-    cfg.dynamicSmemBytes = pl.cfg.smem_bytes;
-    cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    const cudaError_t e = pl.cfg.epi_warps == 8
-                              ? cudaLaunchKernelEx(&cfg, gemm_tn_f16_pair<8>, tmA, tmB, tmD, pl.p)
+  // Programmatic dependent launch: the kernel's set-up (barriers, TMEM)
+  // may overlap the end of the previous kernel in the stream; the kernel
+  // waits for that kernel before its first global-memory access.
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cudaLaunchAttribute attr[2];
+  int nattr = 0;
+  if (pl.cfg.pdl) {
+    attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[nattr].val.programmaticStreamSerializationAllowed = 1;
+    ++nattr;
+  }
+  if (pair) {
+    attr[nattr].id = cudaLaunchAttributeClusterDimension;
+    attr[nattr].val.clusterDim.x = 2;
+    attr[nattr].val.clusterDim.y = 1;
+    attr[nattr].val.clusterDim.z = 1;
+    ++nattr;
+  }
+  cfg.gridDim = dim3(pl.cfg.ctas, 1, 1);
+  cfg.blockDim = dim3(threads_for(pl.cfg.epi_warps), 1, 1);
+  cfg.dynamicSmemBytes = pl.cfg.smem_bytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = nattr;
+  cudaError_t e;
+  if (pair)
+    e = pl.cfg.epi_warps == 8 ? cudaLaunchKernelEx(&cfg, gemm_tn_f16_pair<8>, tmA, tmB, tmD, pl.p)
                               : cudaLaunchKernelEx(&cfg, gemm_tn_f16_pair<4>, tmA, tmB, tmD, pl.p);
-    if (e != cudaSuccess) {
-      cudaGetLastError();
-      return GEMM_ERR_LAUNCH;
-    }
+  else if (pl.p.b_resident)
+    e = pl.cfg.epi_warps == 8
+            ? cudaLaunchKernelEx(&cfg, gemm_tn_f16_persistent<8, true>, tmA, tmB, tmD, pl.p)
+            : cudaLaunchKernelEx(&cfg, gemm_tn_f16_persistent<4, true>, tmA, tmB, tmD, pl.p);
+  else
+    e = pl.cfg.epi_warps == 8
+            ? cudaLaunchKernelEx(&cfg, gemm_tn_f16_persistent<8, false>, tmA, tmB, tmD, pl.p)
+            : cudaLaunchKernelEx(&cfg, gemm_tn_f16_persistent<4, false>, tmA, tmB, tmD, pl.p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_LAUNCH;
   }
   if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
   return GEMM_OK;

@@ -77,6 +77,18 @@ __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
+// Programmatic dependent launch.  launch_dependents lets the next kernel in
+// the stream (if it was launched with programmatic serialization) be
+// scheduled before this one ends; wait blocks until every prerequisite grid
+// has completed and its memory is visible, so it must precede this kernel's
+// first global-memory access.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // 2-D tiled load of one box into shared memory; completion is counted in
 // bytes on `bar`.  x is the innermost (contiguous) coordinate.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint32_t bar, int32_t x,

@@ -143,12 +143,15 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
       uint32_t phase = 0;
       uint32_t issued = 0;
       if (kResident) {
-        // One n-block: every tile multiplies by the same B.  Load all of its
-        // 64-wide K slices once, behind one barrier; the ring carries A only.
+        // Every tile of this CTA multiplies by the same n-block of B (the host
+        // orders tiles n-fastest over a grid that is a multiple of num_n).
+        // Load all of its 64-wide K slices once, behind one barrier; the ring
+        // carries A only.
         const int slices = p.num_k_blocks * p.katoms;
+        const int n_row = static_cast<int>(blockIdx.x % p.num_n_blocks) * p.bn;
         mbar_arrive_expect_tx(bres_bar, p.bres_bytes);
         for (int j = 0; j < slices; ++j)
-          tma_load_2d(base + L.bres + j * p.b_atom_bytes, &tmB, bres_bar, j * kBK, 0);
+          tma_load_2d(base + L.bres + j * p.b_atom_bytes, &tmB, bres_bar, j * kBK, n_row);
       }
       for (int t = blockIdx.x; t < p.num_tiles && !*abort_flag; t += gridDim.x) {
         int mb, nb;
@@ -222,20 +225,20 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
             ok = false;
             break;
           }
-          if (kResident && !b_ready) {  // the resident B, once
-            if (!wait_or_abort(bres_bar, 0, p.timeout_ns, abort_flag, kSiteFull)) {
-              ok = false;
-              break;
-            }
-            b_ready = true;
-          }
-          tc_fence_after_sync();
           const uint32_t a_src = base + L.ring + stage * p.stage_bytes;
           uint32_t b_src = a_src + p.katoms * kABytes;
           if (kResident) {
             const int kb = (k0 + i < p.num_k_blocks) ? k0 + i : k0 + i - p.num_k_blocks;
             b_src = base + L.bres + kb * p.katoms * p.b_atom_bytes;
+            if (!b_ready) {  // the resident B, once
+              if (!wait_or_abort(bres_bar, 0, p.timeout_ns, abort_flag, kSiteFull)) {
+                ok = false;
+                break;
+              }
+              b_ready = true;
+            }
           }
+          tc_fence_after_sync();
           for (int at = 0; at < p.katoms; ++at) {
             const uint64_t a_desc = sw128_kmajor_desc(a_src + at * kABytes);
             const uint64_t b_desc =

@@ -21,6 +21,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr int kMaxDynSmem = 232448;  // 227 KiB opt-in limit per CTA on sm_100-class parts
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+constexpr int kMaxResidentN = 4;  // n-blocks a resident-B plan may have
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -161,7 +162,11 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
     }
     for (int cand = 256; cand >= 32; cand -= 32) {
       if (o.bn && cand != o.bn) continue;
-      if (o.b_resident == 2 && cand < N) continue;  // resident B needs a single n-block
+      // resident B: each CTA keeps one n-block, so few n-blocks, and at
+      // least one CTA for each of them
+      if (o.b_resident == 2 && ((N + cand - 1) / cand > kMaxResidentN ||
+                                (o.max_ctas && (N + cand - 1) / cand > o.max_ctas)))
+        continue;
       // a K x N B is loaded in 64-column boxes: each CTA's share of BN must be whole boxes
       if (b_kn && cand % (kind == GEMM_PATH_PAIR ? 128 : 64) != 0) continue;
       const int bm = (kind == GEMM_PATH_PAIR) ? 2 * kBM : kBM;
@@ -195,13 +200,19 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   // still gets at least 3 stages.
   int katoms = o.katoms ? o.katoms
                         : (stages_that_fit(stage_bytes_for(path, bn, 2), epi_warps) >= 3 ? 2 : 1);
-  // Resident B: with one n-block every tile multiplies by the same B, so a
-  // single-CTA kernel can hold all of it in shared memory and stream only A
-  // -- a third of the bytes per 128 x 256 tile when K = N = 256.  Used when
-  // each CTA has at least two tiles and the ring still gets 3 stages of A.
+  // Resident B: a single-CTA kernel whose tiles all share one n-block holds
+  // that n-block's B (BN x K) in shared memory and streams only A -- a third
+  // of the bytes per 128 x 256 tile when K = N = 256.  With a few n-blocks,
+  // tiles are ordered n-fastest (group_m = 1) over a grid that is a multiple
+  // of num_n, so CTA c only ever meets n-block c % num_n.  Used when each CTA
+  // has at least two tiles and the ring still gets 3 stages of A.
   bool b_resident = false;
   uint32_t bres_bytes = 0;
-  const bool res_possible = path != GEMM_PATH_PAIR && num_n == 1 && !b_kn;
+  int64_t ctas_1 = std::min<int64_t>(tiles, sms);
+  if (o.max_ctas) ctas_1 = std::min<int64_t>(ctas_1, o.max_ctas);
+  const int64_t ctas_res = ctas_1 / num_n * num_n;
+  const bool res_possible = path != GEMM_PATH_PAIR && !b_kn && num_n <= kMaxResidentN &&
+                            ctas_res >= 1 && (num_n == 1 || o.group_m <= 1);
   if (o.b_resident == 2 && !res_possible) return GEMM_ERR_INVALID_VALUE;
   if (res_possible && (o.b_resident == 2 || (o.b_resident == 0 && tiles >= 2 * sms))) {
     const int min_stages = (o.b_resident == 2) ? 2 : 3;
@@ -236,10 +247,10 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
     if (o.max_ctas) pairs = std::min<int64_t>(pairs, std::max(1, o.max_ctas / 2));
     ctas = static_cast<int>(2 * pairs);
   } else {
-    ctas = static_cast<int>(std::min<int64_t>(tiles, sms));
-    if (o.max_ctas) ctas = std::min(ctas, o.max_ctas);
+    ctas = static_cast<int>(b_resident ? ctas_res : ctas_1);
   }
-  const int group_m = o.group_m ? o.group_m : (path == GEMM_PATH_PAIR ? 8 : 16);
+  const int group_m =
+      o.group_m ? o.group_m : (path == GEMM_PATH_PAIR ? 8 : (b_resident && num_n > 1 ? 1 : 16));
   const SmemLayout L = SmemLayout::make(stages, stage_bytes, epi_warps, bres_bytes);
 
   Plan pl;

@@ -102,7 +102,8 @@ def test_rejects_bad_options(binding):
                dict(inject=2), dict(max_ctas=-1), dict(path=binding.PATH_SKINNY),
                dict(katoms=3), dict(katoms=-1), dict(epi_warps=6), dict(epi_warps=16),
                dict(acc_f16=2), dict(b_resident=3), dict(b_resident=-1),
-               dict(b_resident=2, path=binding.PATH_PAIR), dict(b_resident=2, bn=32)]:
+               dict(b_resident=2, path=binding.PATH_PAIR),
+               dict(b_resident=2, bn=32, group_m=4)]:
         o = binding._options(**kw)
         M = 256 if kw.get("path") == binding.PATH_SKINNY else 64
         assert _call(binding, P0, P1, P2, M, 64, 64, o) == binding.GEMM_ERR_INVALID_VALUE, kw
@@ -256,14 +257,24 @@ def test_resident_b_plans(binding):
     cfg = binding.query_config(81920, 256, 256)
     assert cfg["b_resident"] == 1 and cfg["path"] == binding.PATH_SQUARE
     assert cfg["smem_bytes"] <= 232448
-    # off on request, and never for several n-blocks, the pair path or a K x N B
+    # off on request, and never for many n-blocks, the pair path or a K x N B
     assert binding.query_config(81920, 256, 256, b_resident=1)["b_resident"] == 0
     assert binding.query_config(8192, 8192, 8192)["b_resident"] == 0
-    assert binding.query_config(81920, 512, 256)["b_resident"] == 0
+    assert binding.query_config(81920, 4096, 256)["b_resident"] == 0
     assert binding.query_config(81920, 256, 256, b_layout=1)["b_resident"] == 0
     # too few tiles per CTA to pay for loading B up front
     assert binding.query_config(1024, 256, 256)["b_resident"] == 0
-    # forced: the tile is widened to cover N; a B too large for shared memory is refused
-    assert binding.query_config(300, 256, 256, path=1, b_resident=2)["bn"] == 256
+    # a few n-blocks: tiles n-fastest over a grid that is a multiple of num_n,
+    # so every CTA meets a single n-block
+    for shape, opts in [((81920, 512, 256), {}), ((81920, 256, 256), dict(bn=128)),
+                        ((7680, 384, 64), dict(bn=128, b_resident=2)),
+                        ((300, 256, 256), dict(path=1, b_resident=2))]:
+        cfg = binding.query_config(*shape, **opts)
+        num_n = -(-shape[1] // cfg["bn"])
+        assert cfg["b_resident"] == 1 and cfg["ctas"] % num_n == 0, (shape, cfg)
+        assert num_n == 1 or cfg["group_m"] == 1
+    # a rasterisation group that would mix n-blocks on one CTA excludes it
+    assert binding.query_config(81920, 256, 256, bn=128, group_m=4)["b_resident"] == 0
+    # a B too large for shared memory is refused when forced
     with pytest.raises(binding.GemmError):
         binding.query_config(4096, 256, 4096, path=1, b_resident=2)

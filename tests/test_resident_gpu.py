@@ -36,6 +36,23 @@ SHAPES = [(300, 256, 256), (1000, 200, 304), (640, 96, 600), (129, 8, 72), (257,
           (1, 8, 8), (4000, 256, 64)]
 
 
+@pytest.mark.parametrize("M,N,K,bn", [(7680, 384, 64, 128), (4100, 256, 256, 128),
+                                      (2000, 512, 128, 256), (3000, 200, 192, 64)])
+def test_resident_several_n_blocks(lib, gpu, M, N, K, bn):
+    # each CTA keeps the one n-block its tiles share (grid a multiple of num_n)
+    a = synthetic.uniform_pm1(M + 7 * K, (M, K))
+    b = synthetic.uniform_pm1(N + 11 * K, (N, K))
+    cfg = lib.query_config(M, N, K, path=SQUARE, bn=bn, b_resident=2)
+    num_n = -(-N // bn)
+    assert cfg["b_resident"] == 1 and cfg["ctas"] % num_n == 0
+    res = _run(lib, gpu, a, b, path=SQUARE, bn=bn, b_resident=2)
+    st = compare(res, oracle.gemm_tn(a, b), K, a, b)
+    assert st["bad"] == 0, st
+    streamed = _run(lib, gpu, a, b, path=SQUARE, bn=bn, b_resident=1, katoms=cfg["katoms"],
+                    epi_warps=cfg["epi_warps"])
+    assert np.array_equal(res, streamed)
+
+
 @pytest.mark.parametrize("M,N,K", SHAPES)
 def test_resident_matches_oracle_and_streamed(lib, gpu, M, N, K):
     a = synthetic.uniform_pm1(M * 3 + K, (M, K))

@@ -73,7 +73,10 @@ def _check(got, a, b, c, alpha, beta, kn):
 
 
 RAGGED = [(1, 1, 1), (5, 3, 7), (7, 13, 5), (130, 257, 123), (300, 129, 65), (257, 263, 1031),
-          (64, 1001, 9), (129, 9, 300)]
+          (64, 1001, 9), (129, 9, 300),
+          # rows of 127 / 128+ elements: either side of the switch from the
+          # chunk-per-thread copies to the warp-per-row ones
+          (300, 128, 127), (130, 129, 129), (33, 2049, 4097)]
 
 
 @pytest.mark.parametrize("kn", [False, True])

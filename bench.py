@@ -149,23 +149,53 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ CPU oracle
-def oracle_rate(a_bits, b_bits, target_s: float):
-    """Time the oracle on a slice of rows of A sized to about target_s seconds
-    of wall time on this host.  Returns (flop/s, rows, threads, seconds)."""
+def oracle_block(tag, a_bits, b_bits, rows, cols, threads):
+    """The oracle function that matches workload `tag`, on the block of D made
+    of its first `rows` rows and `cols` columns (B sliced to those columns in
+    either layout; C to that block in the scaled form)."""
     import oracle
+    spec = synthetic.WORKLOADS[tag]
+    a = np.ascontiguousarray(a_bits[:rows])
+    if spec.get("b_kn"):
+        b = np.ascontiguousarray(b_bits[:, :cols])
+    else:
+        b = np.ascontiguousarray(b_bits[:cols])
+    if "alpha" in spec:
+        c = np.ascontiguousarray(synthetic.workload_c(tag)[:rows, :cols]) if spec["beta"] else None
+        return lambda: oracle.gemm_scaled(a, b, c, spec["alpha"], spec["beta"],
+                                          bool(spec.get("b_kn")), threads=threads)
+    if spec.get("acc_f16"):
+        return lambda: oracle.gemm_tn_f16acc(a, b, threads=threads)
+    return lambda: oracle.gemm_tn(a, b, threads=threads)
+
+
+def oracle_rate(tag, a_bits, b_bits, target_s: float):
+    """Time the workload's oracle on a slice of rows of D sized to about
+    target_s seconds of wall time on this host.
+    Returns (flop/s, rows, threads, seconds)."""
+    import oracle
+    spec = synthetic.WORKLOADS[tag]
     threads = oracle.default_threads()
-    K = a_bits.shape[1]
-    N = b_bits.shape[0]
+    K, N = spec["K"], spec["N"]
     t0 = time.perf_counter()
-    oracle.gemm_tn(a_bits[:1], b_bits, threads=1)
+    oracle_block(tag, a_bits, b_bits, 1, N, 1)()
     one_row = max(time.perf_counter() - t0, 1e-6)             # seconds for one row, 1 thread
-    rows = int(max(1, min(a_bits.shape[0], round(target_s / one_row) * threads)))
+    rows = int(max(1, min(spec["M"], round(target_s / one_row) * threads)))
     rows = max(threads, (rows // threads) * threads) if rows >= threads else rows
-    rows = min(rows, a_bits.shape[0])
+    rows = min(rows, spec["M"])
+    step = oracle_block(tag, a_bits, b_bits, rows, N, threads)
     t0 = time.perf_counter()
-    oracle.gemm_tn(np.ascontiguousarray(a_bits[:rows]), b_bits, threads=threads)
+    step()
     dt = time.perf_counter() - t0
     return 2.0 * rows * N * K / dt, rows, min(threads, rows), dt
+
+
+def oracle_kind(spec) -> str:
+    if spec.get("acc_f16"):
+        return "oracle with an fp16 accumulator rounded after every 16-deep K slice"
+    if "alpha" in spec:
+        return "full oracle of alpha A op(B) + beta C (double arithmetic, one fp16 rounding)"
+    return "full oracle (double accumulation, one fp16 rounding)"
 
 
 def run_reference(args, tag):
@@ -181,25 +211,24 @@ def run_reference(args, tag):
     # whole run stays near args.reference_budget seconds of wall time
     probe_cols = min(256, spec["N"])
     t0 = time.perf_counter()
-    oracle.gemm_tn(a_bits[:1], np.ascontiguousarray(b_bits[:probe_cols]), threads=1)
+    oracle_block(tag, a_bits, b_bits, 1, probe_cols, 1)()
     per_elem = max(time.perf_counter() - t0, 1e-9) / probe_cols
     budget = max(0.05, args.reference_budget / max(1, args.steps + args.warmup))
     rows = min(spec["M"], threads)
     cols = int(min(spec["N"], max(8, budget * min(threads, rows) / per_elem / rows)))
-    a_slice = np.ascontiguousarray(a_bits[:rows])
-    b_slice = np.ascontiguousarray(b_bits[:cols])
+    step = oracle_block(tag, a_bits, b_bits, rows, cols, threads)
     for _ in range(args.warmup):
-        oracle.gemm_tn(a_slice, b_slice, threads=threads)
+        step()
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        oracle.gemm_tn(a_slice, b_slice, threads=threads)
+        step()
         times.append(time.perf_counter() - t0)
     flops = 2.0 * rows * cols * K
     ms = statistics.mean(times) * 1e3
     value = flops / (ms * 1e-3) / 1e12
     sample = (f"a {rows} x {cols} block of D (of {spec['M']} x {spec['N']}, K={K}) per step, "
-              f"full oracle (double accumulation, one fp16 rounding)")
+              f"{oracle_kind(spec)}")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -617,11 +646,11 @@ def run_gpu(args, tag):
             "clocks": clk,
             "wall_s_timed_region": wall}
     if world == 1 and not args.no_cpu:
-        rate, rows, cores, dt = oracle_rate(a_bits, b_bits, args.cpu_seconds)
+        rate, rows, cores, dt = oracle_rate(tag, a_bits, b_bits, args.cpu_seconds)
         line["cpu_baseline"] = {"value": rate / 1e12, "unit": UNIT, "cores": cores,
                                 "kind": "oracle",
                                 "sample": f"{rows} rows of D ({rows}x{N}, K={K}) in {dt:.1f} s; "
-                                          f"full oracle: double accumulation, one fp16 rounding"}
+                                          f"{oracle_kind(spec)}"}
     print(json.dumps(line))
     return 0
 

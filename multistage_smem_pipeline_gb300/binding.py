@@ -145,8 +145,8 @@ def gemm_tn_f16(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = Non
 
 def gemm_tn_f16_ex(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = None, stream=None,
                    **opts) -> torch.Tensor:
-    """gemm_tn_f16 with explicit options (path, bn, kstage, max_ctas, group_m, timeout_ns,
-    inject, katoms, epi_warps)."""
+    """gemm_tn_f16 with explicit options: path, bn, kstage, max_ctas, group_m, timeout_ns,
+    inject, katoms, epi_warps, acc_f16, b_resident, pdl (the fields of gemm_options_t)."""
     M, N, K, out = _check_operands(a, b, out)
     o = _options(**opts)
     with torch.cuda.device(a.device):

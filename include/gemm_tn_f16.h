@@ -175,7 +175,9 @@ int gemm_f16_padded(void* D, const void* C, const void* A, const void* B, int64_
  * operand it reads or writes is already aligned).  It depends on the
  * pointers' alignment, so pass the pointers of the call (they are not
  * dereferenced).  Host only; returns GEMM_ERR_INVALID_VALUE for a negative
- * or too-large size, a bad b_layout or a NULL `bytes`. */
+ * or too-large size (K or N above 2^31 - 8, or a workspace of 2^63 bytes or
+ * more), a bad b_layout or a NULL `bytes`.  gemm_f16_padded refuses the same
+ * sizes. */
 int gemm_padded_workspace_bytes(const void* D, const void* C, const void* A, const void* B,
                                 int64_t M, int64_t N, int64_t K, float beta, int b_layout,
                                 uint64_t* bytes);

@@ -551,6 +551,7 @@ int run(void* D, const void* A, const void* B, int64_t M, int64_t N, int64_t K,
 // tile multiples before its kernel; here the pad is only what TMA needs.
 
 struct PadPlan {
+  bool ok;              // false: a padded extent or the workspace size would overflow
   int64_t Kp, Np;
   bool pack_a, pack_b, pad_d;
   bool c_to_d;          // C copied into D (D aligned, C not); then C := D (in place)
@@ -570,26 +571,34 @@ PadPlan plan_padding(const void* D, const void* C, const void* A, const void* B,
   std::memset(&pp, 0, sizeof(pp));
   pp.Kp = padded_cols(K);
   pp.Np = padded_cols(N);
-  if (M == 0 || N == 0 || K == 0) return pp;  // nothing reaches the GEMM kernel
+  // the kernel's extents are int32: K and N rounded up to 8 must still fit
+  pp.ok = pp.Kp <= INT_MAX && pp.Np <= INT_MAX;
+  if (!pp.ok || M == 0 || N == 0 || K == 0) return pp;  // nothing reaches the GEMM kernel
   pp.pack_a = !aligned16(A) || K % 8 != 0;
   pp.pack_b = !aligned16(B) || (b_kn ? N % 8 != 0 : K % 8 != 0);
   pp.pad_d = !aligned16(D) || N % 8 != 0;
   pp.c_to_d = !pp.pad_d && beta != 0.0f && !aligned16(C);
+  // Each region is below 2^63 bytes (extents below 2^31); the sum of three
+  // is kept below 2^63 too, or the plan is refused.
   constexpr uint64_t kRegionAlign = 256;
+  constexpr uint64_t kLimit = uint64_t{1} << 63;
   uint64_t off = 0;
+  const auto add = [&](uint64_t bytes) {
+    const uint64_t r = round_up(bytes, kRegionAlign);
+    if (r >= kLimit - off) pp.ok = false;
+    else off += r;
+  };
   if (pp.pack_a) {
     pp.off_a = off;
-    off += round_up(static_cast<uint64_t>(M) * pp.Kp * 2, kRegionAlign);
+    add(static_cast<uint64_t>(M) * pp.Kp * 2);
   }
   if (pp.pack_b) {
     pp.off_b = off;
-    off += round_up(b_kn ? static_cast<uint64_t>(K) * pp.Np * 2
-                         : static_cast<uint64_t>(N) * pp.Kp * 2,
-                    kRegionAlign);
+    add(b_kn ? static_cast<uint64_t>(K) * pp.Np * 2 : static_cast<uint64_t>(N) * pp.Kp * 2);
   }
   if (pp.pad_d) {
     pp.off_d = off;
-    off += round_up(static_cast<uint64_t>(M) * pp.Np * 2, kRegionAlign);
+    add(static_cast<uint64_t>(M) * pp.Np * 2);
   }
   pp.total = off;
   return pp;
@@ -622,6 +631,7 @@ int run_padded(void* D, const void* C, const void* A, const void* B, int64_t M, 
   if ((rc = check_options(opt, b_kn, M, N, K)) != GEMM_OK) return rc;
   if (M == 0 || N == 0) return GEMM_OK;
   const PadPlan pp = plan_padding(D, C, A, B, M, N, K, beta, b_kn);
+  if (!pp.ok) return GEMM_ERR_INVALID_VALUE;
   if (pp.total > 0) {
     if (!workspace || workspace_bytes < pp.total) return GEMM_ERR_INVALID_VALUE;
     if (!aligned16(workspace)) return GEMM_ERR_MISALIGNED;
@@ -692,7 +702,9 @@ extern "C" int gemm_padded_workspace_bytes(const void* D, const void* C, const v
   if (!bytes || M < 0 || N < 0 || K < 0 || M > INT_MAX || N > INT_MAX || K > INT_MAX ||
       (b_layout != 0 && b_layout != 1))
     return GEMM_ERR_INVALID_VALUE;
-  *bytes = plan_padding(D, C, A, B, M, N, K, beta, b_layout).total;
+  const PadPlan pp = plan_padding(D, C, A, B, M, N, K, beta, b_layout);
+  if (!pp.ok) return GEMM_ERR_INVALID_VALUE;
+  *bytes = pp.total;
   return GEMM_OK;
 }
 

@@ -206,6 +206,11 @@ def test_padded_workspace_sizes(binding):
     assert _ws_bytes(binding, P0, 0, P1, P2, 8191, 8191, 8191) == (0, 3 * region)
     E = binding.GEMM_ERR_INVALID_VALUE
     assert _ws_bytes(binding, P0, 0, P1, P2, -1, 16, 16)[0] == E
+    # K or N that rounds up past the kernel's int32 extents, and a workspace
+    # whose size would overflow, are refused
+    assert _ws_bytes(binding, P0, 0, P1, P2, 1, 16, 2**31 - 1)[0] == E
+    assert _ws_bytes(binding, P0, 0, P1, P2, 1, 2**31 - 1, 16)[0] == E
+    assert _ws_bytes(binding, P0 + 2, 0, P1 + 2, P2 + 2, 2**31 - 1, 2**31 - 9, 2**31 - 9)[0] == E
     assert _ws_bytes(binding, P0, 0, P1, P2, 16, 16, 16, layout=2)[0] == E
     assert binding.LIB.gemm_padded_workspace_bytes(P0, 0, P1, P2, 1, 1, 1, 0.0, 0, None) == E
 
@@ -239,6 +244,7 @@ def test_padded_entry_rejects_bad_arguments(binding):
     assert _padded(binding, P0, P0 + 2, P1, P2, 16, 13, 15, ws=W, ws_bytes=need, beta=1.0) == E
     assert _padded(binding, P0, 0, P0 + 64, P2, 16, 13, 15, ws=W, ws_bytes=need) == E
     assert _padded(binding, P0, 0, P1, P2, -3, 13, 15) == E
+    assert _padded(binding, P0, 0, P1, P2, 16, 16, 2**31 - 1) == E
     # empty outputs are no-ops without a workspace or a device
     assert _padded(binding, 0, 0, 0, 0, 0, 13, 15) == binding.GEMM_OK
     assert _padded(binding, P0 + 2, 0, 0, 0, 7, 0, 15) == binding.GEMM_OK

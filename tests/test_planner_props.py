@@ -1,0 +1,91 @@
+"""Planner invariants over many seeded shapes and options (host only, no GPU):
+every plan the library accepts fits the hardware and is self-consistent."""
+import numpy as np
+import pytest
+
+from multistage_smem_pipeline_gb300 import synthetic
+
+SMEM_LIMIT = 232448      # dynamic shared memory per CTA on sm_100-class parts
+TMEM_COLS = 512
+
+
+@pytest.fixture(scope="module")
+def binding():
+    from multistage_smem_pipeline_gb300 import build
+    build.build()
+    from multistage_smem_pipeline_gb300 import binding as b
+    return b
+
+
+def _shapes(n, seed):
+    u = synthetic.uniform01(seed, 3 * n).reshape(n, 3)
+    # log-uniform sizes: M in [1, 2^17], N and K in [8, 2^15], N and K multiples of 8
+    M = np.maximum(1, np.exp2(u[:, 0] * 17)).astype(np.int64)
+    N = np.maximum(1, np.exp2(u[:, 1] * 12)).astype(np.int64) * 8
+    K = np.maximum(1, np.exp2(u[:, 2] * 12)).astype(np.int64) * 8
+    return list(zip(M.tolist(), N.tolist(), K.tolist()))
+
+
+def _check(cfg, M, N, K):
+    assert cfg["smem_bytes"] <= SMEM_LIMIT
+    assert 2 <= cfg["kstage"] <= 16
+    assert cfg["katoms"] in (1, 2) and cfg["bk"] == 64 * cfg["katoms"]
+    assert cfg["epi_warps"] in (4, 8)
+    assert 32 <= cfg["bn"] <= 256 and cfg["bn"] % 32 == 0
+    assert cfg["tmem_cols"] >= 2 * cfg["bn"] and cfg["tmem_cols"] <= TMEM_COLS
+    assert cfg["tmem_cols"] & (cfg["tmem_cols"] - 1) == 0          # a power of two
+    bm = 256 if cfg["path"] == 3 else 128
+    assert cfg["bm"] == bm
+    assert cfg["tiles"] == -(-M // bm) * -(-N // cfg["bn"])
+    assert 1 <= cfg["ctas"] <= cfg["tiles"] * (2 if cfg["path"] == 3 else 1)
+    if cfg["path"] == 3:
+        assert cfg["ctas"] % 2 == 0                                    # whole clusters of 2
+    if cfg["path"] == 2:
+        assert M <= 128
+    if cfg["b_resident"]:
+        num_n = -(-N // cfg["bn"])
+        assert cfg["path"] != 3 and num_n <= 4 and cfg["ctas"] % num_n == 0
+        assert num_n == 1 or cfg["group_m"] == 1
+
+
+def test_default_plans_fit(binding):
+    for M, N, K in _shapes(3000, 501):
+        _check(binding.query_config(M, N, K), M, N, K)
+
+
+@pytest.mark.parametrize("opts", [dict(path=1), dict(path=3), dict(katoms=1), dict(katoms=2),
+                                  dict(epi_warps=4), dict(epi_warps=8), dict(b_resident=1),
+                                  dict(acc_f16=1), dict(b_layout=1), dict(max_ctas=37)])
+def test_forced_plans_fit_or_are_refused(binding, opts):
+    accepted = 0
+    for M, N, K in _shapes(600, 502 + len(str(opts))):
+        try:
+            cfg = binding.query_config(M, N, K, **opts)
+        except binding.GemmError as e:
+            assert e.status == binding.GEMM_ERR_INVALID_VALUE
+            continue
+        accepted += 1
+        _check(cfg, M, N, K)
+        if "path" in opts and opts["path"] == 3:
+            assert cfg["path"] == 3
+        if "katoms" in opts:
+            assert cfg["katoms"] == opts["katoms"]
+        if "epi_warps" in opts:
+            assert cfg["epi_warps"] == opts["epi_warps"]
+        if "max_ctas" in opts:
+            assert cfg["ctas"] <= opts["max_ctas"]
+        if opts.get("b_resident") == 1:
+            assert cfg["b_resident"] == 0
+        if opts.get("b_layout") == 1:
+            assert cfg["bn"] % (128 if cfg["path"] == 3 else 64) == 0 and not cfg["b_resident"]
+    assert accepted > 0
+
+
+def test_every_ring_depth_that_is_offered_fits(binding):
+    for M, N, K in _shapes(200, 503):
+        deepest = binding.query_config(M, N, K)["kstage"]
+        for ks in range(2, deepest + 1):
+            _check(binding.query_config(M, N, K, kstage=ks), M, N, K)
+        if deepest < 16:
+            with pytest.raises(binding.GemmError):
+                binding.query_config(M, N, K, kstage=deepest + 1)

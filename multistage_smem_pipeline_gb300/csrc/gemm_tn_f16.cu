@@ -13,9 +13,19 @@
 
 #include "gemm_pair_kernel.cuh"
 #include "gemm_tn_f16.h"
-#include "repack.cuh"
+#include "host.cuh"
 
 namespace gb300 {
+
+struct DeviceState {
+  bool init = false;
+  int status = GEMM_OK;
+  int sm_count = 0;
+  int smem_attr = 0;       // dynamic smem granted to the single-CTA kernel
+  int pair_smem_attr = 0;  // ... and to the pair kernel
+  int max_pairs = 0;       // co-resident 2-CTA clusters at full shared memory
+};
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -27,15 +37,6 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-struct DeviceState {
-  bool init = false;
-  int status = GEMM_OK;
-  int sm_count = 0;
-  int smem_attr = 0;       // dynamic smem granted to the single-CTA kernel
-  int pair_smem_attr = 0;  // ... and to the pair kernel
-  int max_pairs = 0;       // co-resident 2-CTA clusters at full shared memory
-};
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
@@ -51,33 +52,6 @@ int get_encoder() {
     return GEMM_ERR_CUDA;
   g_encode = reinterpret_cast<EncodeTiledFn>(fn);
   return GEMM_OK;
-}
-
-// Current device, checked to be compute capability 10.3 (state cached).
-int current_device(int* dev_out, DeviceState** st_out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) {
-    cudaGetLastError();
-    return GEMM_ERR_CUDA;
-  }
-  if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_CUDA;
-  std::lock_guard<std::mutex> lk(g_mu);
-  DeviceState& st = g_dev[dev];
-  if (!st.init) {
-    int major = 0, minor = 0, sms = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-      cudaGetLastError();
-      return GEMM_ERR_CUDA;
-    }
-    st.init = true;
-    st.sm_count = sms;
-    st.status = (major == 10 && minor == 3) ? GEMM_OK : GEMM_ERR_UNSUPPORTED_DEVICE;
-  }
-  *dev_out = dev;
-  *st_out = &st;
-  return st.status;
 }
 
 uint32_t pow2_at_least(uint32_t x) {
@@ -302,14 +276,6 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   return GEMM_OK;
 }
 
-// A row-major fp16 matrix as one TMA tensor map sees it: `cols` contiguous
-// elements per row, `rows` rows, `ld` elements between row starts (ld * 2 a
-// multiple of 16, the base 16-byte aligned).
-struct View {
-  const void* ptr;
-  uint64_t cols, rows, ld;
-};
-
 int encode_2d(CUtensorMap* map, const View& v, uint32_t box_inner, uint32_t box_outer,
               CUtensorMapSwizzle swz) {
   const cuuint64_t dims[2] = {v.cols, v.rows};
@@ -368,11 +334,6 @@ int prepare_device(DeviceState* st) {
   return GEMM_OK;
 }
 
-bool overlaps(const void* a, uint64_t abytes, const void* b, uint64_t bbytes) {
-  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
-  return x < y + bbytes && y < x + abytes;
-}
-
 int check_args(const void* D, const void* A, const void* B, int64_t M, int64_t N, int64_t K) {
   if (M < 0 || N < 0 || K < 0 || M > INT_MAX || N > INT_MAX || K > INT_MAX)
     return GEMM_ERR_INVALID_VALUE;
@@ -387,13 +348,6 @@ int check_args(const void* D, const void* A, const void* B, int64_t M, int64_t N
     return GEMM_ERR_INVALID_VALUE;
   return GEMM_OK;
 }
-
-// The scaled form D = alpha * A op(B) + beta * C (nullptr: D = A B^T).
-struct Scaled {
-  const void* C;
-  float alpha, beta;
-  int b_kn;
-};
 
 // D = beta * C elementwise: the scaled form with an empty k range.
 __global__ void scale_c_kernel(uint16_t* D, const uint16_t* C, float beta, int64_t n) {
@@ -417,8 +371,41 @@ int check_scaled(const void* D, const Scaled& sc, int64_t M, int64_t N) {
   return GEMM_OK;
 }
 
-// D = beta * C (rounded to fp16), or D = 0 when beta == 0: the empty sum
-// (K == 0).  Element by element, so any 2-byte alignment is accepted.
+}  // namespace
+
+int current_device(int* dev_out, DeviceState** st_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& st = g_dev[dev];
+  if (!st.init) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return GEMM_ERR_CUDA;
+    }
+    st.init = true;
+    st.sm_count = sms;
+    st.status = (major == 10 && minor == 3) ? GEMM_OK : GEMM_ERR_UNSUPPORTED_DEVICE;
+  }
+  *dev_out = dev;
+  *st_out = &st;
+  return st.status;
+}
+
+int device_sm_count(const DeviceState* st) { return st->sm_count; }
+
+bool overlaps(const void* a, uint64_t abytes, const void* b, uint64_t bbytes) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + bbytes && y < x + abytes;
+}
+
 int write_empty_sum(void* D, const void* C, float beta, int64_t n, int sm_count,
                     cudaStream_t stream) {
   if (C && beta != 0.0f) {
@@ -434,12 +421,6 @@ int write_empty_sum(void* D, const void* C, float beta, int64_t n, int sm_count,
   return GEMM_OK;
 }
 
-// One GEMM launch on aligned operands.  M, N, K are the extents the kernel
-// tiles and iterates; the views give each operand's tensor-map extents and
-// row stride (A: K x M, B: K x N for an N x K B or N x K for a K x N B,
-// D: N x M, as cols x rows).  A view may be narrower than the iterated
-// extent: the loads past its edge read zeros.  sc != nullptr selects the
-// scaled epilogue, reading C with row stride ldc.
 int launch_gemm(int64_t M, int64_t N, int64_t K, const View& a, const View& b, const View& d,
                 int b_kn, const Scaled* sc, int64_t ldc, const gemm_options_t* opt,
                 DeviceState* st, cudaStream_t stream) {
@@ -511,13 +492,14 @@ int launch_gemm(int64_t M, int64_t N, int64_t K, const View& a, const View& b, c
   return GEMM_OK;
 }
 
-// Options are checked against the shape even when there is nothing to compute.
 int check_options(const gemm_options_t* opt, int b_kn, int64_t M, int64_t N, int64_t K) {
   if (!opt) return GEMM_OK;
   Plan tmp;
   return make_plan(std::max<int64_t>(M, 1), std::max<int64_t>(N, 8), std::max<int64_t>(K, 8), opt,
                    148, 74, &tmp, b_kn);
 }
+
+namespace {
 
 int run(void* D, const void* A, const void* B, int64_t M, int64_t N, int64_t K,
         const gemm_options_t* opt, cudaStream_t stream, const Scaled* sc = nullptr) {
@@ -541,144 +523,6 @@ int run(void* D, const void* A, const void* B, int64_t M, int64_t N, int64_t K,
   return launch_gemm(M, N, K, a, b, d, b_kn, sc, N, opt, st, stream);
 }
 
-// ---------------------------------------------------------------- padded path
-//
-// Any K and N and any 2-byte-aligned operand: every operand whose base or
-// row stride is not 16-byte aligned is first copied into a caller-owned
-// workspace with rows padded to a multiple of 8 elements (+0 in the pad),
-// the GEMM runs on the aligned copies, and D is copied back.  This is the
-// host wrapper of "CUDA 算子笔记 2" (GEMM section), which pads A, B and C to
-// tile multiples before its kernel; here the pad is only what TMA needs.
-
-struct PadPlan {
-  bool ok;              // false: a padded extent or the workspace size would overflow
-  int64_t Kp, Np;
-  bool pack_a, pack_b, pad_d;
-  bool c_to_d;          // C copied into D (D aligned, C not); then C := D (in place)
-  uint64_t off_a, off_b, off_d, total;
-};
-
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
-
-uint64_t round_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
-
-// Which operands are repacked and where they go in the workspace.  The pure
-// function of the arguments that both gemm_padded_workspace_bytes and
-// gemm_f16_padded evaluate.
-PadPlan plan_padding(const void* D, const void* C, const void* A, const void* B, int64_t M,
-                     int64_t N, int64_t K, float beta, int b_kn) {
-  PadPlan pp;
-  std::memset(&pp, 0, sizeof(pp));
-  pp.Kp = padded_cols(K);
-  pp.Np = padded_cols(N);
-  // the kernel's extents are int32: K and N rounded up to 8 must still fit
-  pp.ok = pp.Kp <= INT_MAX && pp.Np <= INT_MAX;
-  if (!pp.ok || M == 0 || N == 0 || K == 0) return pp;  // nothing reaches the GEMM kernel
-  pp.pack_a = !aligned16(A) || K % 8 != 0;
-  pp.pack_b = !aligned16(B) || (b_kn ? N % 8 != 0 : K % 8 != 0);
-  pp.pad_d = !aligned16(D) || N % 8 != 0;
-  pp.c_to_d = !pp.pad_d && beta != 0.0f && !aligned16(C);
-  // Each region is below 2^63 bytes (extents below 2^31); the sum of three
-  // is kept below 2^63 too, or the plan is refused.
-  constexpr uint64_t kRegionAlign = 256;
-  constexpr uint64_t kLimit = uint64_t{1} << 63;
-  uint64_t off = 0;
-  const auto add = [&](uint64_t bytes) {
-    const uint64_t r = round_up(bytes, kRegionAlign);
-    if (r >= kLimit - off) pp.ok = false;
-    else off += r;
-  };
-  if (pp.pack_a) {
-    pp.off_a = off;
-    add(static_cast<uint64_t>(M) * pp.Kp * 2);
-  }
-  if (pp.pack_b) {
-    pp.off_b = off;
-    add(b_kn ? static_cast<uint64_t>(K) * pp.Np * 2 : static_cast<uint64_t>(N) * pp.Kp * 2);
-  }
-  if (pp.pad_d) {
-    pp.off_d = off;
-    add(static_cast<uint64_t>(M) * pp.Np * 2);
-  }
-  pp.total = off;
-  return pp;
-}
-
-int check_padded_args(const void* D, const void* C, const void* A, const void* B, int64_t M,
-                      int64_t N, int64_t K, float alpha, float beta, int b_kn) {
-  if (M < 0 || N < 0 || K < 0 || M > INT_MAX || N > INT_MAX || K > INT_MAX)
-    return GEMM_ERR_INVALID_VALUE;
-  if (b_kn != 0 && b_kn != 1) return GEMM_ERR_INVALID_VALUE;
-  if (!std::isfinite(alpha) || !std::isfinite(beta)) return GEMM_ERR_INVALID_VALUE;
-  if (M == 0 || N == 0) return GEMM_OK;
-  if (!D || (K > 0 && (!A || !B)) || (beta != 0.0f && !C)) return GEMM_ERR_INVALID_VALUE;
-  const auto odd = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 1) != 0; };
-  if (odd(D) || (K > 0 && (odd(A) || odd(B))) || (beta != 0.0f && odd(C)))
-    return GEMM_ERR_MISALIGNED;
-  const uint64_t dbytes = static_cast<uint64_t>(M) * N * 2;
-  if (K > 0 && (overlaps(D, dbytes, A, static_cast<uint64_t>(M) * K * 2) ||
-                overlaps(D, dbytes, B, static_cast<uint64_t>(N) * K * 2)))
-    return GEMM_ERR_INVALID_VALUE;
-  if (beta != 0.0f && C != D && overlaps(C, dbytes, D, dbytes)) return GEMM_ERR_INVALID_VALUE;
-  return GEMM_OK;
-}
-
-int run_padded(void* D, const void* C, const void* A, const void* B, int64_t M, int64_t N,
-               int64_t K, float alpha, float beta, int b_kn, void* workspace,
-               uint64_t workspace_bytes, const gemm_options_t* opt, cudaStream_t stream) {
-  int rc = check_padded_args(D, C, A, B, M, N, K, alpha, beta, b_kn);
-  if (rc != GEMM_OK) return rc;
-  if ((rc = check_options(opt, b_kn, M, N, K)) != GEMM_OK) return rc;
-  if (M == 0 || N == 0) return GEMM_OK;
-  const PadPlan pp = plan_padding(D, C, A, B, M, N, K, beta, b_kn);
-  if (!pp.ok) return GEMM_ERR_INVALID_VALUE;
-  if (pp.total > 0) {
-    if (!workspace || workspace_bytes < pp.total) return GEMM_ERR_INVALID_VALUE;
-    if (!aligned16(workspace)) return GEMM_ERR_MISALIGNED;
-    const uint64_t dbytes = static_cast<uint64_t>(M) * N * 2;
-    if (overlaps(workspace, pp.total, D, dbytes) ||
-        (beta != 0.0f && overlaps(workspace, pp.total, C, dbytes)) ||
-        (K > 0 && (overlaps(workspace, pp.total, A, static_cast<uint64_t>(M) * K * 2) ||
-                   overlaps(workspace, pp.total, B, static_cast<uint64_t>(N) * K * 2))))
-      return GEMM_ERR_INVALID_VALUE;
-  }
-  int dev = 0;
-  DeviceState* st = nullptr;
-  if ((rc = current_device(&dev, &st)) != GEMM_OK) return rc;
-  if (K == 0) return write_empty_sum(D, C, beta, M * N, st->sm_count, stream);
-
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  const int sms = st->sm_count;
-  const auto ok = [](cudaError_t e) { return e == cudaSuccess; };
-  if (pp.pack_a && !ok(repack_rows(ws + pp.off_a, A, M, K, sms, stream))) return GEMM_ERR_LAUNCH;
-  if (pp.pack_b && !ok(b_kn ? repack_rows(ws + pp.off_b, B, K, N, sms, stream)
-                            : repack_rows(ws + pp.off_b, B, N, K, sms, stream)))
-    return GEMM_ERR_LAUNCH;
-  // Where C is read it ends up aligned with row stride ldc: in the padded D
-  // (which the GEMM then updates in place), in D itself, or as given.
-  void* d_eff = pp.pad_d ? static_cast<void*>(ws + pp.off_d) : D;
-  const void* c_eff = C;
-  if (beta != 0.0f && (pp.pad_d || pp.c_to_d)) {
-    if (!ok(repack_rows(d_eff, C, M, N, sms, stream))) return GEMM_ERR_LAUNCH;
-    c_eff = d_eff;
-  }
-  const uint64_t m = M, n = N, k = K, kp = pp.Kp, np = pp.Np;
-  // With K padded, A's pad columns are +0 and the kernel iterates Kp; an
-  // unpacked B (K x N) simply ends at row K and reads zeros past it.
-  const View a = pp.pack_a ? View{ws + pp.off_a, kp, m, kp} : View{A, k, m, k};
-  View b;
-  if (b_kn)
-    b = pp.pack_b ? View{ws + pp.off_b, np, k, np} : View{B, n, k, n};
-  else
-    b = pp.pack_b ? View{ws + pp.off_b, kp, n, kp} : View{B, k, n, k};
-  const View d = pp.pad_d ? View{d_eff, np, m, np} : View{D, n, m, n};
-  const Scaled sc{c_eff, alpha, beta, b_kn};
-  rc = launch_gemm(M, N, pp.Kp, a, b, d, b_kn, &sc, pp.pad_d ? pp.Np : N, opt, st, stream);
-  if (rc != GEMM_OK) return rc;
-  if (pp.pad_d && !ok(unpack_rows(D, d_eff, M, N, sms, stream))) return GEMM_ERR_LAUNCH;
-  return GEMM_OK;
-}
-
 }  // namespace
 }  // namespace gb300
 
@@ -694,26 +538,6 @@ extern "C" int gemm_f16_scaled(void* D, const void* C, const void* A, const void
                                const gemm_options_t* opt, void* stream) {
   const Scaled sc{C, alpha, beta, b_layout};
   return run(D, A, B, M, N, K, opt, static_cast<cudaStream_t>(stream), &sc);
-}
-
-extern "C" int gemm_padded_workspace_bytes(const void* D, const void* C, const void* A,
-                                           const void* B, int64_t M, int64_t N, int64_t K,
-                                           float beta, int b_layout, uint64_t* bytes) {
-  if (!bytes || M < 0 || N < 0 || K < 0 || M > INT_MAX || N > INT_MAX || K > INT_MAX ||
-      (b_layout != 0 && b_layout != 1))
-    return GEMM_ERR_INVALID_VALUE;
-  const PadPlan pp = plan_padding(D, C, A, B, M, N, K, beta, b_layout);
-  if (!pp.ok) return GEMM_ERR_INVALID_VALUE;
-  *bytes = pp.total;
-  return GEMM_OK;
-}
-
-extern "C" int gemm_f16_padded(void* D, const void* C, const void* A, const void* B, int64_t M,
-                               int64_t N, int64_t K, float alpha, float beta, int b_layout,
-                               void* workspace, uint64_t workspace_bytes,
-                               const gemm_options_t* opt, void* stream) {
-  return run_padded(D, C, A, B, M, N, K, alpha, beta, b_layout, workspace, workspace_bytes, opt,
-                    static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int gemm_tn_f16_ex(void* D, const void* A, const void* B, int64_t M, int64_t N,

@@ -141,12 +141,15 @@ int gemm_f16_scaled(void* D, const void* C, const void* A, const void* B, int64_
  * kernel and copying the result back.
  *
  * Same operation, layouts (leading dimensions K or N, rows packed back to
- * back) and ownership as gemm_f16_scaled.  Each operand whose base address
- * or row stride is not a multiple of 16 bytes is first copied, on `stream`,
- * into `workspace` with its rows padded to a multiple of 8 elements (+0 in
- * the pad); the GEMM kernel then runs on the aligned copies, and a padded D
- * is copied back into D.  Operands already aligned are used in place, so
- * with K % 8 == 0, N % 8 == 0 and 16-byte-aligned pointers this is exactly
+ * back) and ownership as gemm_f16_scaled.  Each operand the kernel reads
+ * whose base address or row stride is not a multiple of 16 bytes is first
+ * copied, on `stream`, into `workspace` with its rows padded to a multiple
+ * of 8 elements (+0 in the pad); the GEMM kernel then runs on the aligned
+ * copies.  A D of that kind is written by the kernel's epilogue with plain
+ * stores when beta == 0; when beta != 0 the GEMM updates a padded copy of C
+ * in place, which is then copied into D.  Operands already aligned are used
+ * in place, so with K % 8 == 0, N % 8 == 0 and 16-byte-aligned pointers this
+ * is exactly
  * gemm_f16_scaled and needs no workspace.  The results are those of the
  * unpadded problem: the pad contributes exact zeros.
  *
@@ -163,9 +166,9 @@ int gemm_f16_scaled(void* D, const void* C, const void* A, const void* B, int64_
  * a workspace that is too small or overlaps an operand is
  * GEMM_ERR_INVALID_VALUE, and a misaligned one GEMM_ERR_MISALIGNED; the
  * other checks are those of gemm_f16_scaled.  Nothing is launched when a
- * check fails.  Up to four kernels are launched (repack A, repack B, the
- * GEMM -- after a repack of C where C is read -- and the copy back of D),
- * all asynchronous on `stream`.
+ * check fails.  Up to five kernels are launched (repack A, repack B, repack
+ * C when C is read into a padded D, the GEMM, and then the copy back of that
+ * D), all asynchronous on `stream`.
  */
 int gemm_f16_padded(void* D, const void* C, const void* A, const void* B, int64_t M, int64_t N,
                     int64_t K, float alpha, float beta, int b_layout, void* workspace,

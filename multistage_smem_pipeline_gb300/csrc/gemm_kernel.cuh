@@ -65,8 +65,10 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uin
 }
 
 // kResident selects the resident-B mode at compile time (p.b_resident must
-// agree), so the streaming kernel's loops carry none of its code.
-template <int kEpiWarps, bool kResident>
+// agree), so the streaming kernel's loops carry none of its code.  kDirectD
+// stores D with plain stores to p.D (row stride p.ldd) instead of TMA stores
+// through tmD, which such kernels never touch.
+template <int kEpiWarps, bool kResident, bool kDirectD>
 __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
     gemm_tn_f16_persistent(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
@@ -113,7 +115,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    tma_prefetch_desc(&tmD);
+    if (!kDirectD) tma_prefetch_desc(&tmD);
   }
   __syncwarp();  // reconverge warp 0 before the aligned CTA barrier
   __syncthreads();  // barriers initialised: the producer may start loading at once
@@ -323,11 +325,17 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
                        pack_half2(r[8 * j + 4], r[8 * j + 5]),
                        pack_half2(r[8 * j + 6], r[8 * j + 7]));
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_2d(&tmD, buf, n0 + c * kEpiCols, m0);
-          bulk_commit_group();
+        if (kDirectD) {
+          __syncwarp();
+          store_chunk_direct(buf, p.D, p.ldd, p.M, p.N, m0, n0 + c * kEpiCols, lane);
+          __syncwarp();
+        } else {
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmD, buf, n0 + c * kEpiCols, m0);
+            bulk_commit_group();
+          }
         }
         ++chunk_seq;
       }

@@ -33,7 +33,8 @@
 
 namespace gb300 {
 
-template <int kEpiWarps>
+// kDirectD: as in gemm_tn_f16_persistent.
+template <int kEpiWarps, bool kDirectD>
 __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
     gemm_tn_f16_pair(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB,
@@ -79,7 +80,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    tma_prefetch_desc(&tmD);
+    if (!kDirectD) tma_prefetch_desc(&tmD);
   }
   __syncwarp();
   // Both CTAs' barriers exist before any remote arrive or multicast commit,
@@ -253,11 +254,17 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
                        pack_half2(r[8 * j + 4], r[8 * j + 5]),
                        pack_half2(r[8 * j + 6], r[8 * j + 7]));
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_2d(&tmD, buf, n0 + c * kEpiCols, m0);
-          bulk_commit_group();
+        if (kDirectD) {
+          __syncwarp();
+          store_chunk_direct(buf, p.D, p.ldd, p.M, p.N, m0, n0 + c * kEpiCols, lane);
+          __syncwarp();
+        } else {
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmD, buf, n0 + c * kEpiCols, m0);
+            bulk_commit_group();
+          }
         }
         ++chunk_seq;
       }

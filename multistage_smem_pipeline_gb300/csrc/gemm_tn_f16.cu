@@ -289,24 +289,46 @@ int encode_2d(CUtensorMap* map, const View& v, uint32_t box_inner, uint32_t box_
   return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_INVALID_VALUE;
 }
 
-// Grant both kernels the full dynamic shared memory and find how many
+template <typename Kernel>
+bool grant_smem(Kernel k) {
+  return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem) ==
+         cudaSuccess;
+}
+
+// Every kernel instantiation: epilogue warps (4, 8) x resident B x direct D
+// store for the single-CTA kernel, epilogue warps x direct D for the pair.
+template <bool kDirectD>
+bool grant_all(bool ok) {
+  return ok && grant_smem(gemm_tn_f16_persistent<4, false, kDirectD>) &&
+         grant_smem(gemm_tn_f16_persistent<8, false, kDirectD>) &&
+         grant_smem(gemm_tn_f16_persistent<4, true, kDirectD>) &&
+         grant_smem(gemm_tn_f16_persistent<8, true, kDirectD>) &&
+         grant_smem(gemm_tn_f16_pair<4, kDirectD>) && grant_smem(gemm_tn_f16_pair<8, kDirectD>);
+}
+
+template <bool kDirectD>
+cudaError_t launch_kernel(const cudaLaunchConfig_t& cfg, bool pair, bool resident, int epi_warps,
+                          const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d,
+                          const GemmParams& p) {
+  if (pair)
+    return epi_warps == 8 ? cudaLaunchKernelEx(&cfg, gemm_tn_f16_pair<8, kDirectD>, a, b, d, p)
+                          : cudaLaunchKernelEx(&cfg, gemm_tn_f16_pair<4, kDirectD>, a, b, d, p);
+  if (resident)
+    return epi_warps == 8
+               ? cudaLaunchKernelEx(&cfg, gemm_tn_f16_persistent<8, true, kDirectD>, a, b, d, p)
+               : cudaLaunchKernelEx(&cfg, gemm_tn_f16_persistent<4, true, kDirectD>, a, b, d, p);
+  return epi_warps == 8
+             ? cudaLaunchKernelEx(&cfg, gemm_tn_f16_persistent<8, false, kDirectD>, a, b, d, p)
+             : cudaLaunchKernelEx(&cfg, gemm_tn_f16_persistent<4, false, kDirectD>, a, b, d, p);
+}
+
+// Grant every kernel the full dynamic shared memory and find how many
 // 2-CTA clusters can be resident at once (the pair path's persistent grid).
 int prepare_device(DeviceState* st) {
   std::lock_guard<std::mutex> lk(g_mu);
   if (st->smem_attr == kMaxDynSmem && st->pair_smem_attr == kMaxDynSmem && st->max_pairs > 0)
     return GEMM_OK;
-  if (cudaFuncSetAttribute(gemm_tn_f16_persistent<4, false>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem) != cudaSuccess ||
-      cudaFuncSetAttribute(gemm_tn_f16_persistent<8, false>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem) != cudaSuccess ||
-      cudaFuncSetAttribute(gemm_tn_f16_persistent<4, true>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem) != cudaSuccess ||
-      cudaFuncSetAttribute(gemm_tn_f16_persistent<8, true>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem) != cudaSuccess ||
-      cudaFuncSetAttribute(gemm_tn_f16_pair<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kMaxDynSmem) != cudaSuccess ||
-      cudaFuncSetAttribute(gemm_tn_f16_pair<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kMaxDynSmem) != cudaSuccess) {
+  if (!grant_all<true>(grant_all<false>(true))) {
     cudaGetLastError();
     return GEMM_ERR_CUDA;
   }
@@ -325,7 +347,8 @@ int prepare_device(DeviceState* st) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&clusters, gemm_tn_f16_pair<8>, &cfg) != cudaSuccess ||
+  if (cudaOccupancyMaxActiveClusters(&clusters, gemm_tn_f16_pair<8, false>, &cfg) !=
+          cudaSuccess ||
       clusters < 1) {
     cudaGetLastError();
     clusters = st->sm_count / 2;
@@ -423,7 +446,7 @@ int write_empty_sum(void* D, const void* C, float beta, int64_t n, int sm_count,
 
 int launch_gemm(int64_t M, int64_t N, int64_t K, const View& a, const View& b, const View& d,
                 int b_kn, const Scaled* sc, int64_t ldc, const gemm_options_t* opt,
-                DeviceState* st, cudaStream_t stream) {
+                DeviceState* st, cudaStream_t stream, uint16_t* d_direct, int64_t ldd) {
   int rc;
   if ((rc = prepare_device(st)) != GEMM_OK) return rc;
   Plan pl;
@@ -443,9 +466,15 @@ int launch_gemm(int64_t M, int64_t N, int64_t K, const View& a, const View& b, c
   CUtensorMap tmA, tmB, tmD;
   const int b_rc = b_kn ? encode_2d(&tmB, b, 64, kBK, CU_TENSOR_MAP_SWIZZLE_128B)
                         : encode_2d(&tmB, b, kBK, b_box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
-  if (encode_2d(&tmA, a, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B) != GEMM_OK || b_rc != GEMM_OK ||
-      encode_2d(&tmD, d, kEpiCols, 32, CU_TENSOR_MAP_SWIZZLE_64B) != GEMM_OK)
+  if (encode_2d(&tmA, a, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B) != GEMM_OK || b_rc != GEMM_OK)
     return GEMM_ERR_INVALID_VALUE;
+  if (d_direct) {  // plain stores to D; the kernel never reads tmD
+    pl.p.D = d_direct;
+    pl.p.ldd = ldd;
+    tmD = tmA;
+  } else if (encode_2d(&tmD, d, kEpiCols, 32, CU_TENSOR_MAP_SWIZZLE_64B) != GEMM_OK) {
+    return GEMM_ERR_INVALID_VALUE;
+  }
 
   // Programmatic dependent launch: the kernel's set-up (barriers, TMEM)
   // may overlap the end of the previous kernel in the stream; the kernel
@@ -472,18 +501,11 @@ int launch_gemm(int64_t M, int64_t N, int64_t K, const View& a, const View& b, c
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = nattr;
-  cudaError_t e;
-  if (pair)
-    e = pl.cfg.epi_warps == 8 ? cudaLaunchKernelEx(&cfg, gemm_tn_f16_pair<8>, tmA, tmB, tmD, pl.p)
-                              : cudaLaunchKernelEx(&cfg, gemm_tn_f16_pair<4>, tmA, tmB, tmD, pl.p);
-  else if (pl.p.b_resident)
-    e = pl.cfg.epi_warps == 8
-            ? cudaLaunchKernelEx(&cfg, gemm_tn_f16_persistent<8, true>, tmA, tmB, tmD, pl.p)
-            : cudaLaunchKernelEx(&cfg, gemm_tn_f16_persistent<4, true>, tmA, tmB, tmD, pl.p);
-  else
-    e = pl.cfg.epi_warps == 8
-            ? cudaLaunchKernelEx(&cfg, gemm_tn_f16_persistent<8, false>, tmA, tmB, tmD, pl.p)
-            : cudaLaunchKernelEx(&cfg, gemm_tn_f16_persistent<4, false>, tmA, tmB, tmD, pl.p);
+  const cudaError_t e =
+      d_direct ? launch_kernel<true>(cfg, pair, pl.p.b_resident != 0, pl.cfg.epi_warps, tmA, tmB,
+                                     tmD, pl.p)
+               : launch_kernel<false>(cfg, pair, pl.p.b_resident != 0, pl.cfg.epi_warps, tmA, tmB,
+                                      tmD, pl.p);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return GEMM_ERR_LAUNCH;

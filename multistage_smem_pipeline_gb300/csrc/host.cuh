@@ -48,9 +48,12 @@ int check_options(const gemm_options_t* opt, int b_kn, int64_t M, int64_t N, int
 // row stride (A: K x M, B: K x N for an N x K B or N x K for a K x N B,
 // D: N x M, as cols x rows).  A view may be narrower than the iterated
 // extent: the loads past its edge read zeros.  sc != nullptr selects the
-// scaled epilogue, reading C with row stride ldc.
+// scaled epilogue, reading C with row stride ldc.  d_direct != nullptr
+// stores D with plain stores there (row stride ldd, any 2-byte alignment)
+// instead of TMA stores through the view d, which is then not used.
 int launch_gemm(int64_t M, int64_t N, int64_t K, const View& a, const View& b, const View& d,
                 int b_kn, const Scaled* sc, int64_t ldc, const gemm_options_t* opt,
-                DeviceState* st, cudaStream_t stream);
+                DeviceState* st, cudaStream_t stream, uint16_t* d_direct = nullptr,
+                int64_t ldd = 0);
 
 }  // namespace gb300

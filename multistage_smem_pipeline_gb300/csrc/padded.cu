@@ -1,10 +1,13 @@
 // The padded entry point: gemm_f16_scaled for any K and N and any
-// 2-byte-aligned operand.  Every operand whose base or row stride is not
-// 16-byte aligned is first copied into a caller-owned workspace with rows
-// padded to a multiple of 8 elements (+0 in the pad), the GEMM runs on the
-// aligned copies, and D is copied back.  This is the host wrapper of "CUDA 算子
-// 笔记 2" (GEMM section), which pads A, B and C to tile multiples before its
-// kernel; here the pad is only what TMA needs.
+// 2-byte-aligned operand.  Every operand the GEMM kernel reads whose base or
+// row stride is not 16-byte aligned is first copied into a caller-owned
+// workspace with rows padded to a multiple of 8 elements (+0 in the pad) and
+// the GEMM runs on the aligned copies.  A D of that kind is stored by the
+// kernel's epilogue with plain stores when C is not read; when C is read, C
+// goes into a padded D that the GEMM updates in place and that is copied back
+// afterwards.  This is the host wrapper of "CUDA 算子笔记 2" (GEMM section),
+// which pads A, B and C to tile multiples before its kernel; here the pad is
+// only what TMA needs.
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -23,6 +26,7 @@ struct PadPlan {
   bool ok;              // false: a padded extent or the workspace size would overflow
   int64_t Kp, Np;
   bool pack_a, pack_b, pad_d;
+  bool direct_d;        // pad_d and C not read: the GEMM stores D directly, no padded copy
   bool c_to_d;          // C copied into D (D aligned, C not); then C := D (in place)
   uint64_t off_a, off_b, off_d, total;
 };
@@ -46,6 +50,7 @@ PadPlan plan_padding(const void* D, const void* C, const void* A, const void* B,
   pp.pack_a = !aligned16(A) || K % 8 != 0;
   pp.pack_b = !aligned16(B) || (b_kn ? N % 8 != 0 : K % 8 != 0);
   pp.pad_d = !aligned16(D) || N % 8 != 0;
+  pp.direct_d = pp.pad_d && beta == 0.0f;
   pp.c_to_d = !pp.pad_d && beta != 0.0f && !aligned16(C);
   // Each region is below 2^63 bytes (extents below 2^31); the sum of three
   // is kept below 2^63 too, or the plan is refused.
@@ -65,7 +70,7 @@ PadPlan plan_padding(const void* D, const void* C, const void* A, const void* B,
     pp.off_b = off;
     add(b_kn ? static_cast<uint64_t>(K) * pp.Np * 2 : static_cast<uint64_t>(N) * pp.Kp * 2);
   }
-  if (pp.pad_d) {
+  if (pp.pad_d && !pp.direct_d) {
     pp.off_d = off;
     add(static_cast<uint64_t>(M) * pp.Np * 2);
   }
@@ -125,9 +130,10 @@ int run_padded(void* D, const void* C, const void* A, const void* B, int64_t M, 
     return GEMM_ERR_LAUNCH;
   // Where C is read it ends up aligned with row stride ldc: in the padded D
   // (which the GEMM then updates in place), in D itself, or as given.
-  void* d_eff = pp.pad_d ? static_cast<void*>(ws + pp.off_d) : D;
+  const bool padded_copy = pp.pad_d && !pp.direct_d;
+  void* d_eff = padded_copy ? static_cast<void*>(ws + pp.off_d) : D;
   const void* c_eff = C;
-  if (beta != 0.0f && (pp.pad_d || pp.c_to_d)) {
+  if (beta != 0.0f && (padded_copy || pp.c_to_d)) {
     if (!ok(repack_rows(d_eff, C, M, N, sms, stream))) return GEMM_ERR_LAUNCH;
     c_eff = d_eff;
   }
@@ -140,11 +146,12 @@ int run_padded(void* D, const void* C, const void* A, const void* B, int64_t M, 
     b = pp.pack_b ? View{ws + pp.off_b, np, k, np} : View{B, n, k, n};
   else
     b = pp.pack_b ? View{ws + pp.off_b, kp, n, kp} : View{B, k, n, k};
-  const View d = pp.pad_d ? View{d_eff, np, m, np} : View{D, n, m, n};
+  const View d = padded_copy ? View{d_eff, np, m, np} : View{D, n, m, n};
   const Scaled sc{c_eff, alpha, beta, b_kn};
-  rc = launch_gemm(M, N, pp.Kp, a, b, d, b_kn, &sc, pp.pad_d ? pp.Np : N, opt, st, stream);
+  rc = launch_gemm(M, N, pp.Kp, a, b, d, b_kn, &sc, padded_copy ? pp.Np : N, opt, st, stream,
+                   pp.direct_d ? static_cast<uint16_t*>(D) : nullptr, N);
   if (rc != GEMM_OK) return rc;
-  if (pp.pad_d && !ok(unpack_rows(D, d_eff, M, N, sms, stream))) return GEMM_ERR_LAUNCH;
+  if (padded_copy && !ok(unpack_rows(D, d_eff, M, N, sms, stream))) return GEMM_ERR_LAUNCH;
   return GEMM_OK;
 }
 

@@ -51,6 +51,8 @@ struct GemmParams {
   int32_t b_resident;    // 1: all of B (one n-block, every k slice) is loaded once per CTA
                          //    into its own region; the ring then carries A only
   uint32_t bres_bytes;   // size of that region: num_k_blocks * katoms * b_atom_bytes (else 0)
+  uint16_t* D;           // direct-store kernels only: D (rows not 16-byte aligned) ...
+  int64_t ldd;           // ... and its row stride in elements
 };
 
 // MN-major B: one 64-element N chunk per TMA box; chunks 8 KiB apart.
@@ -152,6 +154,32 @@ __device__ __forceinline__ void apply_alpha_beta(uint32_t (&r)[32], const GemmPa
             __float_as_uint(fmaf(p.beta, f.y, __uint_as_float(r[8 * g + 2 * q + 1])));
       }
     }
+  }
+}
+
+__device__ __forceinline__ uint16_t ld_shared_u16(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// The direct-store form of the epilogue's last step, for a D whose rows are
+// not 16-byte aligned (no TMA store can describe them): the warp writes the
+// 32 x 32 chunk it staged at `buf` (64-byte rows, piece j of row r at
+// position j ^ ((r >> 1) & 3)) row by row, lane l taking column l, so each
+// store instruction writes one row's 64 contiguous bytes.  Rows at or past M
+// and columns at or past N are not written.
+__device__ __forceinline__ void store_chunk_direct(uint32_t buf, uint16_t* D, int64_t ldd, int M,
+                                                   int N, int m0, int n0, int lane) {
+  const int col = n0 + lane;
+  const uint32_t piece = static_cast<uint32_t>(lane) >> 3;
+  const uint32_t within = (static_cast<uint32_t>(lane) & 7u) * 2u;
+#pragma unroll 4
+  for (int r = 0; r < 32; ++r) {
+    const uint32_t sw = (static_cast<uint32_t>(r) >> 1) & 3u;
+    const uint16_t v = ld_shared_u16(buf + static_cast<uint32_t>(r) * 64u + ((piece ^ sw) << 4) + within);
+    const int row = m0 + r;
+    if (row < M && col < N) D[static_cast<int64_t>(row) * ldd + col] = v;
   }
 }
 

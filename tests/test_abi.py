@@ -188,12 +188,16 @@ def test_padded_workspace_sizes(binding):
     assert _ws_bytes(binding, P0, P1, P1 + 4096, P2, 10, 16, 16, beta=1.0) == (0, 0)
     # K = 15: A (10 x 16) and an N x K B (16 x 16) repacked, 256-byte regions
     assert _ws_bytes(binding, P0, 0, P1, P2, 10, 16, 15) == (0, 512 + 512)
-    # N = 13 with a K x N B: B (16 x 16) and D (10 x 16) padded; A as given
-    assert _ws_bytes(binding, P0, 0, P1, P2, 10, 13, 16, layout=1) == (0, 512 + 512)
+    # N = 13 with a K x N B: B (16 x 16) repacked; A as given; D is stored
+    # directly by the kernel (C not read), so it needs no region
+    assert _ws_bytes(binding, P0, 0, P1, P2, 10, 13, 16, layout=1) == (0, 512)
     # ... while an N x K B (13 x 16) is aligned as it is
-    assert _ws_bytes(binding, P0, 0, P1, P2, 10, 13, 16, layout=0) == (0, 512)
-    # a base address alone forces a repack of that operand
-    assert _ws_bytes(binding, P0 + 2, 0, P1, P2, 10, 16, 16) == (0, 512)
+    assert _ws_bytes(binding, P0, 0, P1, P2, 10, 13, 16, layout=0) == (0, 0)
+    # with C read, D (10 x 16 padded) holds C during the GEMM
+    assert _ws_bytes(binding, P0, P1 + 8192, P2, P2 + 65536, 10, 13, 16, beta=1.0) == (0, 512)
+    assert _ws_bytes(binding, P0 + 2, P1 + 8192, P2, P2 + 65536, 10, 16, 16, beta=1.0) == (0, 512)
+    # a base address alone forces a repack of that operand it reads
+    assert _ws_bytes(binding, P0 + 2, 0, P1, P2, 10, 16, 16) == (0, 0)
     assert _ws_bytes(binding, P0, 0, P1 + 6, P2, 10, 16, 16) == (0, 512)
     assert _ws_bytes(binding, P0, 0, P1, P2 + 4, 300, 16, 16) == (0, 512)
     # a misaligned C with an aligned D is copied into D: no region of its own
@@ -201,9 +205,11 @@ def test_padded_workspace_sizes(binding):
     # nothing reaches the GEMM kernel: no workspace
     assert _ws_bytes(binding, P0 + 2, 0, P1 + 2, P2 + 2, 10, 13, 0) == (0, 0)
     assert _ws_bytes(binding, P0 + 2, 0, P1 + 2, P2 + 2, 0, 13, 7) == (0, 0)
-    # large sizes: 8191^3 repacks A, B and D, each 8191 x 8192 fp16
+    # large sizes: 8191^3 repacks A and B, each 8191 x 8192 fp16 (D is stored
+    # directly); with C read, D's padded copy adds a third region
     region = (8191 * 8192 * 2 + 255) // 256 * 256
-    assert _ws_bytes(binding, P0, 0, P1, P2, 8191, 8191, 8191) == (0, 3 * region)
+    assert _ws_bytes(binding, P0, 0, P1, P2, 8191, 8191, 8191) == (0, 2 * region)
+    assert _ws_bytes(binding, P0, 1 << 40, P1, P2, 8191, 8191, 8191, beta=0.5) == (0, 3 * region)
     E = binding.GEMM_ERR_INVALID_VALUE
     assert _ws_bytes(binding, P0, 0, P1, P2, -1, 16, 16)[0] == E
     # K or N that rounds up past the kernel's int32 extents, and a workspace

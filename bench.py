@@ -371,7 +371,8 @@ def run_gpu(args, tag):
     stream = torch.cuda.current_stream(dev)
     opts = {"path": ["auto", "square", "skinny", "pair"].index(args.path), "bn": args.bn,
             "kstage": args.kstage, "katoms": args.katoms, "group_m": args.group_m,
-            "epi_warps": args.epi_warps, "b_resident": args.b_resident, "pdl": args.pdl}
+            "epi_warps": args.epi_warps, "b_resident": args.b_resident, "pdl": args.pdl,
+            "wide": args.wide}
     forced = any(opts.values())
     cfg = binding.query_config(M, N, K, b_layout=1 if spec.get("b_kn") else 0, **opts)
 
@@ -614,7 +615,8 @@ def run_gpu(args, tag):
             iso["frac_of_burst_peak"] = iso["tflops_clean_flush"] / float(peaks["bf16_tflops"])
     direct_d = padded and spec["N"] % 8 != 0     # a padded call with unaligned D rows, C not read
     flag = lambda x: "true" if x else "false"
-    roof["kernel"] = ("gemm_tn_f16_pair<%d, %s>" % (cfg["epi_warps"], flag(direct_d))
+    roof["kernel"] = ("gemm_tn_f16_pair<%d, %s, %d>" % (cfg["epi_warps"], flag(direct_d),
+                                                        2 if cfg["wide"] else 1)
                       if cfg["path"] == 3 else
                       "gemm_tn_f16_persistent<%d, %s, %s>" % (cfg["epi_warps"],
                                                               flag(cfg["b_resident"]),
@@ -646,7 +648,7 @@ def run_gpu(args, tag):
                 "path": ["auto", "square", "skinny", "pair"][cfg["path"]], "bm": cfg["bm"],
                 "bn": cfg["bn"], "bk": cfg["bk"], "kstage": cfg["kstage"], "ctas": cfg["ctas"],
                 "tiles": cfg["tiles"], "katoms": cfg["katoms"], "epi_warps": cfg["epi_warps"],
-                "b_resident": cfg["b_resident"], "pdl": cfg["pdl"],
+                "b_resident": cfg["b_resident"], "pdl": cfg["pdl"], "wide": cfg["wide"],
                 "forced": forced}),
             "launch_ms": ({"mean": ms, "median": statistics.median(launches_ms),
                            "p10": float(np.percentile(launches_ms, 10)),
@@ -709,6 +711,8 @@ def main():
                     help="diagnostics: resident B (0 choose, 1 never, 2 always)")
     ap.add_argument("--pdl", type=int, default=0, choices=[0, 1],
                     help="diagnostics: 1 = launch without programmatic dependent launch")
+    ap.add_argument("--wide", type=int, default=0, choices=[0, 1, 2],
+                    help="diagnostics: pair units of two n-tiles (0 choose, 1 never, 2 always)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

@@ -97,6 +97,12 @@ typedef struct {
                           kernel's set-up overlaps the end of the previous kernel
                           in the stream; it waits for that kernel -- griddepcontrol
                           -- before touching global memory); 1: plain launch */
+  int wide;            /* pair path: 0 = choose, 1 = never, 2 = always (on another
+                          path GEMM_ERR_INVALID_VALUE).  A wide unit is two adjacent
+                          n-tiles (a 256 x 2*bn block) sharing each A slice: the
+                          ring carries A once per two B halves and both TMEM
+                          accumulators hold the unit, so the same shared memory
+                          holds a deeper ring.  Results are bit-identical. */
 } gemm_options_t;
 
 /* gemm_tn_f16 with an explicit configuration (sweeps, tests).  Same
@@ -194,6 +200,8 @@ typedef struct {
   int epi_warps;       /* threads per CTA = 64 + 32 * epi_warps */
   int b_resident;      /* 1: B is held in shared memory for the whole kernel */
   int pdl;             /* 1: launched with programmatic stream serialization */
+  int wide;            /* 1: pair units of two adjacent n-tiles (tiles still counts
+                          output tiles; the grid is sized by units) */
 } gemm_config_t;
 int gemm_query_config(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt,
                       gemm_config_t* out);

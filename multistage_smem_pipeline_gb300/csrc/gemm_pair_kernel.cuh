@@ -34,7 +34,18 @@
 namespace gb300 {
 
 // kDirectD: as in gemm_tn_f16_persistent.
-template <int kEpiWarps, bool kDirectD>
+// kNT: n-tiles per work unit.  With 2 (the "wide" unit), one unit is the
+// 256 x 2*BN block of two adjacent n-tiles: every ring stage carries the A
+// slice once and both tiles' B halves, the MMA thread issues both tiles'
+// MMAs from it into the two TMEM accumulators, and the epilogue drains the
+// first accumulator, then the second.  A k-slice's bytes then feed twice the
+// MMA work, so the same shared memory holds a deeper ring (4 one-slice
+// stages of 48 KiB instead of 3 two-slice stages of 64 KiB at BN = 256):
+// more lookahead against the DRAM latency of a slice's first fetch.  The
+// accumulators are no longer double-buffered across units: the next unit's
+// MMAs wait until both are drained.  Each accumulator sees the same MMAs in
+// the same order as with kNT = 1, so the results are bit-identical.
+template <int kEpiWarps, bool kDirectD, int kNT>
 __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
     gemm_tn_f16_pair(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB,
@@ -45,6 +56,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
   uint8_t* const smem = smem_raw + (base - raw);
   constexpr int kThreads = threads_for(kEpiWarps);
   constexpr int kChunkStride = kEpiWarps / 4;  // warps sharing a TMEM lane quadrant
+  constexpr int kEpiBatch = 4;                  // TMEM chunks read per wait in the epilogue
   const SmemLayout L = SmemLayout::make(p.stages, p.stage_bytes, kEpiWarps);
 
   const int warp = threadIdx.x >> 5;
@@ -108,7 +120,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
         int mb, nb;
         tile_coords(t, p, mb, nb);           // mb counts 256-row pair blocks
         const int a_row = mb * (2 * kBM) + static_cast<int>(rank) * kBM;
-        const int b_row = nb * p.bn + static_cast<int>(rank) * half_bn;
+        const int b_row = nb * kNT * p.bn + static_cast<int>(rank) * half_bn;
         bool ok = true;
         const int k0 = first_k_block(t, p);
         for (int i = 0; i < p.num_k_blocks; ++i) {
@@ -124,18 +136,23 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
           if (!(p.inject == 1 && issued == 0 && rank == 0)) {
             for (int at = 0; at < p.katoms; ++at) {
               const int x = (kb * p.katoms + at) * kBK;  // past K: the box reads zeros
-              const uint32_t ad = a_dst + at * kABytes, bd = b_dst + at * p.b_atom_bytes;
+              const uint32_t ad = a_dst + at * kABytes;
               if (p.l2_hints & 2u)
                 tma_load_2d_pair_hint(ad, &tmA, leader_full, x, a_row, pol_a);
               else
                 tma_load_2d_pair(ad, &tmA, leader_full, x, a_row);
-              if (p.b_kn) {  // B is K x N: one 64-column box per chunk of this CTA's half
-                for (int ch = 0; ch < half_bn / 64; ++ch)
-                  tma_load_2d_pair(bd + ch * kMnChunkBytes, &tmB, leader_full, b_row + 64 * ch, x);
-              } else if (p.l2_hints & 1u) {
-                tma_load_2d_pair_hint(bd, &tmB, leader_full, x, b_row, pol_b);
-              } else {
-                tma_load_2d_pair(bd, &tmB, leader_full, x, b_row);
+#pragma unroll
+              for (int j = 0; j < kNT; ++j) {  // tile j's B half (past N: the box reads zeros)
+                const uint32_t bd = b_dst + (j * p.katoms + at) * p.b_atom_bytes;
+                const int br = b_row + j * p.bn;
+                if (p.b_kn) {  // B is K x N: one 64-column box per chunk of this CTA's half
+                  for (int ch = 0; ch < half_bn / 64; ++ch)
+                    tma_load_2d_pair(bd + ch * kMnChunkBytes, &tmB, leader_full, br + 64 * ch, x);
+                } else if (p.l2_hints & 1u) {
+                  tma_load_2d_pair_hint(bd, &tmB, leader_full, x, br, pol_b);
+                } else {
+                  tma_load_2d_pair(bd, &tmB, leader_full, x, br);
+                }
               }
             }
           }
@@ -162,9 +179,11 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       for (int t = pair; t < p.num_tiles; t += num_pairs) {
-        if (!wait_or_abort(tempty_bar(acc), acc_phase ^ 1u, p.timeout_ns, abort_flag,
-                           kSiteTmemEmpty))
-          break;
+        bool drained = true;
+        for (int j = 0; j < kNT && drained; ++j)
+          drained = wait_or_abort(tempty_bar(acc + j), acc_phase ^ 1u, p.timeout_ns, abort_flag,
+                                  kSiteTmemEmpty);
+        if (!drained) break;
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * p.bn);
         bool ok = true;
@@ -178,13 +197,18 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
           const uint32_t b_src = a_src + p.katoms * kABytes;
           for (int at = 0; at < p.katoms; ++at) {
             const uint64_t a_desc = sw128_kmajor_desc(a_src + at * kABytes);
-            const uint64_t b_desc =
-                p.b_kn ? sw128_mnmajor_desc(b_src + at * p.b_atom_bytes, kMnChunkBytes)
-                       : sw128_kmajor_desc(b_src + at * p.b_atom_bytes);
+            uint64_t b_desc[kNT];
+#pragma unroll
+            for (int j = 0; j < kNT; ++j) {
+              const uint32_t bs = b_src + (j * p.katoms + at) * p.b_atom_bytes;
+              b_desc[j] = p.b_kn ? sw128_mnmajor_desc(bs, kMnChunkBytes) : sw128_kmajor_desc(bs);
+            }
 #pragma unroll
             for (int k = 0; k < kBK / kUmmaK; ++k)
-              umma_f16_pair(d_tmem, a_desc + 2u * k, b_desc + b_kstep * k, p.idesc,
-                            (i | at | k) != 0);
+#pragma unroll
+              for (int j = 0; j < kNT; ++j)
+                umma_f16_pair(d_tmem + static_cast<uint32_t>(j * p.bn), a_desc + 2u * k,
+                              b_desc[j] + b_kstep * k, p.idesc, (i | at | k) != 0);
           }
           umma_commit_pair_mc(empty_bar(stage), 0x3);
           if (++stage == S) {
@@ -194,7 +218,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
         }
         if (!ok) break;
         umma_commit_pair_mc(tfull_bar(acc), 0x3);
-        if (++acc == 2) {
+        if (kNT == 2 || ++acc == 2) {  // a wide unit uses both accumulators
           acc = 0;
           acc_phase ^= 1u;
         }
@@ -222,58 +246,74 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
       if (!ok) break;
       tc_fence_after_sync();
       const int m0 = mb * (2 * kBM) + static_cast<int>(rank) * kBM + q * 32;
-      const int n0 = nb * p.bn;
       const bool rows_live = m0 < p.M;
-      const int nchunks = (min(p.bn, p.N - n0) + kEpiCols - 1) / kEpiCols;
-      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                             static_cast<uint32_t>(acc * p.bn);
-      const uint32_t leader_tempty = mapa_shared(tempty_bar(acc), 0);
-      const int last_c = last_epi_chunk(nchunks, half, kChunkStride);
-      for (int c = half; c <= last_c && rows_live; c += kChunkStride) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(t_row + c * kEpiCols, r);
-        tmem_ld_wait();
-        if (c == last_c) {
+#pragma unroll 1
+      for (int j = 0; j < kNT; ++j) {  // the unit's tiles, one accumulator each
+        const int n0 = (nb * kNT + j) * p.bn;
+        // <= 0 when the tile lies past N (the second tile of a ragged wide unit)
+        const int nchunks = (min(p.bn, p.N - n0) + kEpiCols - 1) / kEpiCols;
+        const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                               static_cast<uint32_t>((acc + j) * p.bn);
+        const uint32_t leader_tempty = mapa_shared(tempty_bar(acc + j), 0);
+        const int last_c = last_epi_chunk(nchunks, half, kChunkStride);
+        // TMEM is read kEpiBatch chunks at a time with one wait, and the
+        // accumulator is released as soon as its last chunk is in registers:
+        // the conversion, the C update and the stores that follow no longer
+        // hold up the next unit's MMAs.
+        for (int c0 = half; c0 <= last_c && rows_live; c0 += kChunkStride * kEpiBatch) {
+          uint32_t r[kEpiBatch][32];
+#pragma unroll
+          for (int b = 0; b < kEpiBatch; ++b)
+            if (c0 + b * kChunkStride <= last_c)
+              tmem_ld_32x32b_x32(t_row + (c0 + b * kChunkStride) * kEpiCols, r[b]);
+          tmem_ld_wait();
+          if (c0 + (kEpiBatch - 1) * kChunkStride >= last_c) {  // the last chunk is in this batch
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(leader_tempty);
+          }
+#pragma unroll
+          for (int b = 0; b < kEpiBatch; ++b) {
+            const int c = c0 + b * kChunkStride;
+            if (c > last_c) break;
+            if (p.acc_f16) widen_f16_accumulator(r[b]);
+            if (p.scaled) apply_alpha_beta(r[b], p, m0 + lane, n0 + c * kEpiCols);
+            const uint32_t buf = my_bufs + (chunk_seq % kEpiBufs) * kEpiChunkBytes;
+            if (chunk_seq >= static_cast<uint32_t>(kEpiBufs)) {
+              if (lane == 0) bulk_wait_group_read<kEpiBufs - 1>();
+              __syncwarp();
+            }
+            const uint32_t row_addr = buf + lane * 64u;
+            const uint32_t sw = (lane >> 1) & 3u;
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              st_shared_v4(row_addr + ((v ^ sw) << 4), pack_half2(r[b][8 * v + 0], r[b][8 * v + 1]),
+                           pack_half2(r[b][8 * v + 2], r[b][8 * v + 3]),
+                           pack_half2(r[b][8 * v + 4], r[b][8 * v + 5]),
+                           pack_half2(r[b][8 * v + 6], r[b][8 * v + 7]));
+            }
+            if (kDirectD) {
+              __syncwarp();
+              store_chunk_direct(buf, p.D, p.ldd, p.M, p.N, m0, n0 + c * kEpiCols, lane);
+              __syncwarp();
+            } else {
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&tmD, buf, n0 + c * kEpiCols, m0);
+                bulk_commit_group();
+              }
+            }
+            ++chunk_seq;
+          }
+        }
+        if (!rows_live || last_c < 0) {
           tc_fence_before_sync();
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(leader_tempty);
         }
-        if (p.acc_f16) widen_f16_accumulator(r);
-        if (p.scaled) apply_alpha_beta(r, p, m0 + lane, n0 + c * kEpiCols);
-        const uint32_t buf = my_bufs + (chunk_seq % kEpiBufs) * kEpiChunkBytes;
-        if (chunk_seq >= static_cast<uint32_t>(kEpiBufs)) {
-          if (lane == 0) bulk_wait_group_read<kEpiBufs - 1>();
-          __syncwarp();
-        }
-        const uint32_t row_addr = buf + lane * 64u;
-        const uint32_t sw = (lane >> 1) & 3u;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          st_shared_v4(row_addr + ((j ^ sw) << 4), pack_half2(r[8 * j + 0], r[8 * j + 1]),
-                       pack_half2(r[8 * j + 2], r[8 * j + 3]),
-                       pack_half2(r[8 * j + 4], r[8 * j + 5]),
-                       pack_half2(r[8 * j + 6], r[8 * j + 7]));
-        }
-        if (kDirectD) {
-          __syncwarp();
-          store_chunk_direct(buf, p.D, p.ldd, p.M, p.N, m0, n0 + c * kEpiCols, lane);
-          __syncwarp();
-        } else {
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&tmD, buf, n0 + c * kEpiCols, m0);
-            bulk_commit_group();
-          }
-        }
-        ++chunk_seq;
       }
-      if (!rows_live || last_c < 0) {
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(leader_tempty);
-      }
-      if (++acc == 2) {
+      if (kNT == 2 || ++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
       }

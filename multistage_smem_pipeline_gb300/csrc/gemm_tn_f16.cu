@@ -32,6 +32,7 @@ constexpr int kMaxDevices = 64;
 constexpr int kMaxDynSmem = 232448;  // 227 KiB opt-in limit per CTA on sm_100-class parts
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 constexpr int kMaxResidentN = 4;  // n-blocks a resident-B plan may have
+constexpr int64_t kWideMinK = 4096;  // shortest k loop for which wide pair units are chosen
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -84,8 +85,16 @@ int stages_that_fit(uint32_t stage_bytes, int epi_warps, uint32_t bres_bytes = 0
 // for its 128 x n x 64 block (8192 flop/clk/SM), and the stage must be
 // refilled at the rate the ring sustains with every SM loading -- about
 // 60 B/clk per SM measured on GB300 with a 4-6 deep ring.
-double kblock_cost(int n_per_sm, uint32_t stage_bytes) {
-  return std::max(2.0 * n_per_sm, static_cast<double>(stage_bytes) / 60.0);
+// With `mmas` > 0 the MMA side is also floored at kMmaIssueCycles per
+// instruction: the issuing thread needs about that long per tcgen05.mma
+// (measured issue to issue), so a 128 x n x 16 MMA with n/2 < 124 cycles of
+// tensor work is issue-bound.  Applied to the pair path, where it decides
+// between tile widths (measured: wide units at bn 160-192 ran at 0.7x of bn
+// 256); the single-CTA plans for short k loops were measured without it.
+constexpr double kMmaIssueCycles = 124.0;
+double kblock_cost(int n_per_sm, uint32_t stage_bytes, int mmas = 0) {
+  const double mma = std::max(2.0 * n_per_sm, mmas * kMmaIssueCycles);
+  return std::max(mma, static_cast<double>(stage_bytes) / 60.0);
 }
 
 uint32_t b_atom_bytes_for(int path, int bn) {
@@ -93,8 +102,9 @@ uint32_t b_atom_bytes_for(int path, int bn) {
   return static_cast<uint32_t>(b_rows) * 128u;
 }
 
-uint32_t stage_bytes_for(int path, int bn, int katoms = 1) {
-  return static_cast<uint32_t>(katoms) * (kABytes + b_atom_bytes_for(path, bn));
+// nt: n-tiles sharing each A slice (2 for a wide pair unit)
+uint32_t stage_bytes_for(int path, int bn, int katoms = 1, int nt = 1) {
+  return static_cast<uint32_t>(katoms) * (kABytes + nt * b_atom_bytes_for(path, bn));
 }
 
 struct Plan {
@@ -110,21 +120,28 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   if (o.path < 0 || o.path > 3 || o.bn < 0 || o.bn > 256 || (o.bn % 32) != 0 || o.kstage < 0 ||
       o.kstage == 1 || o.kstage > kMaxStages || o.max_ctas < 0 || o.group_m < 0 || o.inject < 0 ||
       o.inject > 1 || o.katoms < 0 || o.katoms > 2 || o.acc_f16 < 0 || o.acc_f16 > 1 ||
-      o.b_resident < 0 || o.b_resident > 2 || o.pdl < 0 || o.pdl > 1 ||
+      o.b_resident < 0 || o.b_resident > 2 || o.pdl < 0 || o.pdl > 1 || o.wide < 0 ||
+      o.wide > 2 ||
       (o.epi_warps != 0 && o.epi_warps != 4 && o.epi_warps != 8))
     return GEMM_ERR_INVALID_VALUE;
   if (o.path == GEMM_PATH_SKINNY && M > kBM) return GEMM_ERR_INVALID_VALUE;
   if (max_pairs < 1) max_pairs = std::max(1, sms / 2);
 
-  // Candidates: (path, bn).  Cost = waves x k-blocks x per-k-block cost; ties
-  // go to the pair path, then to the wider tile (less L2 traffic).
-  int path = 0, bn = 0;
+  // Candidates: (path, bn, tiles per unit).  Cost = waves of units x
+  // k-blocks x per-k-block cost; ties go to the pair path, then to wide
+  // units, then to the wider tile (less L2 traffic).  Wide pair units (two
+  // adjacent n-tiles sharing each A slice) are candidates only for long k
+  // loops, where the ring's lookahead, not the per-unit drain, limits the pair.
+  if (o.wide == 2 && o.path != GEMM_PATH_AUTO && o.path != GEMM_PATH_PAIR)
+    return GEMM_ERR_INVALID_VALUE;
+  int path = 0, bn = 0, nt = 1;
   double best = 0;
   for (int cp = 3; cp >= 1; --cp) {
     if (cp == GEMM_PATH_SKINNY) continue;
     int kind = cp;
-    if (o.path != GEMM_PATH_AUTO) {
-      const int want = (o.path == GEMM_PATH_SKINNY) ? GEMM_PATH_SQUARE : o.path;
+    if (o.path != GEMM_PATH_AUTO || o.wide == 2) {  // wide units exist on the pair path only
+      const int want = (o.wide == 2) ? GEMM_PATH_PAIR
+                                     : (o.path == GEMM_PATH_SKINNY) ? GEMM_PATH_SQUARE : o.path;
       if (kind != want) continue;
     } else if (kind == GEMM_PATH_PAIR && (M <= kBM || K <= 1024)) {
       // M <= 128: a pair tile would be at least half empty.  K <= 1024: the
@@ -144,15 +161,27 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
       // a K x N B is loaded in 64-column boxes: each CTA's share of BN must be whole boxes
       if (b_kn && cand % (kind == GEMM_PATH_PAIR ? 128 : 64) != 0) continue;
       const int bm = (kind == GEMM_PATH_PAIR) ? 2 * kBM : kBM;
-      const int64_t tiles = ((M + bm - 1) / bm) * ((N + cand - 1) / cand);
-      const int64_t slots = (kind == GEMM_PATH_PAIR) ? max_pairs : sms;
-      const int64_t waves = (tiles + slots - 1) / slots;
-      const double cost = static_cast<double>(waves) * static_cast<double>((K + kBK - 1) / kBK) *
-                          kblock_cost(cand, stage_bytes_for(kind, cand));
-      if (bn == 0 || cost < best * (1.0 - 1e-9)) {
-        best = cost;
-        bn = cand;
-        path = kind;
+      const int64_t cand_n = (N + cand - 1) / cand;
+      int64_t slots = (kind == GEMM_PATH_PAIR) ? max_pairs : sms;
+      if (kind == GEMM_PATH_PAIR && o.max_ctas)
+        slots = std::min<int64_t>(slots, std::max(1, o.max_ctas / 2));
+      for (int cnt = 2; cnt >= 1; --cnt) {
+        if (cnt == 2 && (kind != GEMM_PATH_PAIR || o.wide == 1 ||
+                         (o.wide == 0 && (cand_n < 2 || K < kWideMinK))))
+          continue;
+        if (cnt == 1 && kind == GEMM_PATH_PAIR && o.wide == 2) continue;
+        const int64_t units = ((M + bm - 1) / bm) * ((cand_n + cnt - 1) / cnt);
+        const int64_t waves = (units + slots - 1) / slots;
+        const double cost = static_cast<double>(waves) *
+                            static_cast<double>((K + kBK - 1) / kBK) *
+                            kblock_cost(cnt * cand, stage_bytes_for(kind, cand, 1, cnt),
+                                        kind == GEMM_PATH_PAIR ? 4 * cnt : 0);
+        if (bn == 0 || cost < best * (1.0 - 1e-9)) {
+          best = cost;
+          bn = cand;
+          path = kind;
+          nt = cnt;
+        }
       }
     }
   }
@@ -164,16 +193,25 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   const int64_t num_n = (N + bn - 1) / bn;
   const int64_t tiles = num_m * num_n;
   if (tiles > INT_MAX) return GEMM_ERR_INVALID_VALUE;
+  // Wide pair units: two adjacent n-tiles per unit share each A slice, so a
+  // one-slice stage feeds twice the MMA work and the ring gets deeper (more
+  // lookahead against DRAM latency) in the same shared memory.
+  const bool wide = nt == 2;
+  const int64_t units_n = (num_n + nt - 1) / nt;
+  const int64_t units = num_m * units_n;
   // Eight epilogue warps drain a tile twice as fast; they pay off when the k
   // loop per tile is short (the epilogue is then the critical path), four
   // are enough -- and leave the MMA and producer warps their issue slots --
   // when it is long.
-  int epi_warps = o.epi_warps ? o.epi_warps : (K <= 1024 ? 8 : 4);
+  // A wide unit releases each accumulator as soon as its chunks are in
+  // registers; eight warps hold all of a quadrant's chunks at once.
+  int epi_warps = o.epi_warps ? o.epi_warps : ((K <= 1024 || wide) ? 8 : 4);
   // Two 64-wide K slices per stage halve the issuing threads' per-byte
   // barrier/commit work (measured: +12 % at 8192^3); used whenever the ring
   // still gets at least 3 stages.
   int katoms = o.katoms ? o.katoms
-                        : (stages_that_fit(stage_bytes_for(path, bn, 2), epi_warps) >= 3 ? 2 : 1);
+                        : (stages_that_fit(stage_bytes_for(path, bn, 2, nt), epi_warps) >= 3 ? 2
+                                                                                         : 1);
   // Resident B: a single-CTA kernel whose tiles all share one n-block holds
   // that n-block's B (BN x K) in shared memory and streams only A -- a third
   // of the bytes per 128 x 256 tile when K = N = 256.  With a few n-blocks,
@@ -210,21 +248,22 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   }
   const int64_t num_k = (K + kBK * katoms - 1) / (kBK * katoms);
   const uint32_t stage_bytes = b_resident ? static_cast<uint32_t>(katoms) * kABytes
-                                          : stage_bytes_for(path, bn, katoms);
+                                          : stage_bytes_for(path, bn, katoms, nt);
   const int fit = stages_that_fit(stage_bytes, epi_warps, bres_bytes);
   if (fit < 2) return GEMM_ERR_INVALID_VALUE;
   const int stages = o.kstage ? o.kstage : fit;
   if (stages > fit) return GEMM_ERR_INVALID_VALUE;
   int ctas;
   if (path == GEMM_PATH_PAIR) {
-    int64_t pairs = std::min<int64_t>(tiles, max_pairs);
+    int64_t pairs = std::min<int64_t>(units, max_pairs);
     if (o.max_ctas) pairs = std::min<int64_t>(pairs, std::max(1, o.max_ctas / 2));
     ctas = static_cast<int>(2 * pairs);
   } else {
     ctas = static_cast<int>(b_resident ? ctas_res : ctas_1);
   }
   const int group_m =
-      o.group_m ? o.group_m : (path == GEMM_PATH_PAIR ? 8 : (b_resident && num_n > 1 ? 1 : 16));
+      o.group_m ? o.group_m
+                : (path == GEMM_PATH_PAIR ? (wide ? 16 : 8) : (b_resident && num_n > 1 ? 1 : 16));
   const SmemLayout L = SmemLayout::make(stages, stage_bytes, epi_warps, bres_bytes);
 
   Plan pl;
@@ -243,6 +282,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   pl.cfg.tmem_cols = static_cast<int>(pow2_at_least(2u * bn));
   pl.cfg.b_resident = b_resident ? 1 : 0;
   pl.cfg.pdl = o.pdl ? 0 : 1;
+  pl.cfg.wide = wide ? 1 : 0;
 
   GemmParams& p = pl.p;
   p.M = static_cast<int32_t>(M);
@@ -251,9 +291,10 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   p.bn = bn;
   p.stages = stages;
   p.num_m_blocks = static_cast<int32_t>(num_m);
-  p.num_n_blocks = static_cast<int32_t>(num_n);
+  // the kernel schedules units: with wide units, pairs of adjacent n-tiles
+  p.num_n_blocks = static_cast<int32_t>(units_n);
   p.num_k_blocks = static_cast<int32_t>(num_k);
-  p.num_tiles = static_cast<int32_t>(tiles);
+  p.num_tiles = static_cast<int32_t>(units);
   p.group_m = group_m;
   p.idesc = make_idesc(bm, bn) | (b_kn ? (1u << 16) : 0u);  // bit 16: B is MN-major
   if (o.acc_f16) p.idesc &= ~(3u << 4);                      // bits 4-5: D format F16
@@ -296,23 +337,33 @@ bool grant_smem(Kernel k) {
 }
 
 // Every kernel instantiation: epilogue warps (4, 8) x resident B x direct D
-// store for the single-CTA kernel, epilogue warps x direct D for the pair.
+// store for the single-CTA kernel, epilogue warps x direct D x tiles per unit
+// for the pair.
 template <bool kDirectD>
 bool grant_all(bool ok) {
   return ok && grant_smem(gemm_tn_f16_persistent<4, false, kDirectD>) &&
          grant_smem(gemm_tn_f16_persistent<8, false, kDirectD>) &&
          grant_smem(gemm_tn_f16_persistent<4, true, kDirectD>) &&
          grant_smem(gemm_tn_f16_persistent<8, true, kDirectD>) &&
-         grant_smem(gemm_tn_f16_pair<4, kDirectD>) && grant_smem(gemm_tn_f16_pair<8, kDirectD>);
+         grant_smem(gemm_tn_f16_pair<4, kDirectD, 1>) &&
+         grant_smem(gemm_tn_f16_pair<8, kDirectD, 1>) &&
+         grant_smem(gemm_tn_f16_pair<4, kDirectD, 2>) && grant_smem(gemm_tn_f16_pair<8, kDirectD, 2>);
+}
+
+template <bool kDirectD, int kNT>
+cudaError_t launch_pair(const cudaLaunchConfig_t& cfg, int epi_warps, const CUtensorMap& a,
+                        const CUtensorMap& b, const CUtensorMap& d, const GemmParams& p) {
+  return epi_warps == 8 ? cudaLaunchKernelEx(&cfg, gemm_tn_f16_pair<8, kDirectD, kNT>, a, b, d, p)
+                        : cudaLaunchKernelEx(&cfg, gemm_tn_f16_pair<4, kDirectD, kNT>, a, b, d, p);
 }
 
 template <bool kDirectD>
-cudaError_t launch_kernel(const cudaLaunchConfig_t& cfg, bool pair, bool resident, int epi_warps,
-                          const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d,
-                          const GemmParams& p) {
+cudaError_t launch_kernel(const cudaLaunchConfig_t& cfg, bool pair, bool wide, bool resident,
+                          int epi_warps, const CUtensorMap& a, const CUtensorMap& b,
+                          const CUtensorMap& d, const GemmParams& p) {
   if (pair)
-    return epi_warps == 8 ? cudaLaunchKernelEx(&cfg, gemm_tn_f16_pair<8, kDirectD>, a, b, d, p)
-                          : cudaLaunchKernelEx(&cfg, gemm_tn_f16_pair<4, kDirectD>, a, b, d, p);
+    return wide ? launch_pair<kDirectD, 2>(cfg, epi_warps, a, b, d, p)
+                : launch_pair<kDirectD, 1>(cfg, epi_warps, a, b, d, p);
   if (resident)
     return epi_warps == 8
                ? cudaLaunchKernelEx(&cfg, gemm_tn_f16_persistent<8, true, kDirectD>, a, b, d, p)
@@ -347,7 +398,7 @@ int prepare_device(DeviceState* st) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&clusters, gemm_tn_f16_pair<8, false>, &cfg) !=
+  if (cudaOccupancyMaxActiveClusters(&clusters, gemm_tn_f16_pair<8, false, 1>, &cfg) !=
           cudaSuccess ||
       clusters < 1) {
     cudaGetLastError();
@@ -501,11 +552,11 @@ int launch_gemm(int64_t M, int64_t N, int64_t K, const View& a, const View& b, c
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = nattr;
+  const bool wide = pl.cfg.wide != 0, res = pl.p.b_resident != 0;
   const cudaError_t e =
-      d_direct ? launch_kernel<true>(cfg, pair, pl.p.b_resident != 0, pl.cfg.epi_warps, tmA, tmB,
-                                     tmD, pl.p)
-               : launch_kernel<false>(cfg, pair, pl.p.b_resident != 0, pl.cfg.epi_warps, tmA, tmB,
-                                      tmD, pl.p);
+      d_direct
+          ? launch_kernel<true>(cfg, pair, wide, res, pl.cfg.epi_warps, tmA, tmB, tmD, pl.p)
+          : launch_kernel<false>(cfg, pair, wide, res, pl.cfg.epi_warps, tmA, tmB, tmD, pl.p);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return GEMM_ERR_LAUNCH;

@@ -103,7 +103,8 @@ def test_rejects_bad_options(binding):
                dict(katoms=3), dict(katoms=-1), dict(epi_warps=6), dict(epi_warps=16),
                dict(acc_f16=2), dict(b_resident=3), dict(b_resident=-1),
                dict(b_resident=2, path=binding.PATH_PAIR),
-               dict(b_resident=2, bn=32, group_m=4)]:
+               dict(b_resident=2, bn=32, group_m=4), dict(wide=3), dict(wide=-1),
+               dict(wide=2, path=binding.PATH_SQUARE)]:
         o = binding._options(**kw)
         M = 256 if kw.get("path") == binding.PATH_SKINNY else 64
         assert _call(binding, P0, P1, P2, M, 64, 64, o) == binding.GEMM_ERR_INVALID_VALUE, kw
@@ -140,9 +141,13 @@ def test_query_config_plans(binding):
                 with pytest.raises(binding.GemmError):
                     binding.query_config(1024, 1024, 1024, kstage=deepest + 1, **q)
     # a pair stage holds half of B, so the pair ring is deeper at the same width
-    assert binding.query_config(4096, 4096, 4096, path=binding.PATH_PAIR, bn=256, katoms=1)[
-        "kstage"] > binding.query_config(4096, 4096, 4096, path=binding.PATH_SQUARE, bn=256,
-                                         katoms=1)["kstage"]
+    assert binding.query_config(4096, 4096, 4096, path=binding.PATH_PAIR, bn=256, katoms=1,
+                                wide=1)["kstage"] > \
+        binding.query_config(4096, 4096, 4096, path=binding.PATH_SQUARE, bn=256,
+                             katoms=1)["kstage"]
+    # a wide pair stage holds A once for two tiles' B halves: the deepest ring at bn 256
+    wide = binding.query_config(8192, 8192, 8192, path=binding.PATH_PAIR, bn=256, wide=2)
+    assert wide["wide"] == 1 and wide["katoms"] == 1 and wide["kstage"] == 4
     # two K slices per stage only where the ring keeps at least 3 stages
     for shape in [(8192, 8192, 8192), (128, 14336, 4096), (256, 256, 256)]:
         cc = binding.query_config(*shape)

@@ -1,7 +1,7 @@
 """Seeded random shapes and options through the C-ABI against the oracle: the
 plain, scaled and padded entries, both B layouts, both kernel paths, forced
-tile widths, ring depths, slices per stage, epilogue warps, resident B and
-the fp16 accumulator."""
+tile widths, ring depths, slices per stage, epilogue warps, resident B, wide
+pair units and the fp16 accumulator."""
 import numpy as np
 import pytest
 import torch
@@ -22,7 +22,7 @@ def lib(gpu):
 
 def _case(i):
     """Shape, entry and options of case i, drawn from a seeded stream."""
-    u = synthetic.uniform01(7000 + i, 16)
+    u = synthetic.uniform01(7000 + i, 17)
     pick = lambda x, options: options[min(int(x * len(options)), len(options) - 1)]
     entry = pick(u[0], ["plain", "scaled", "padded"])
     kn = entry != "plain" and u[1] < 0.5
@@ -49,6 +49,8 @@ def _case(i):
         opts["acc_f16"] = 1
     if u[13] < 0.2:
         opts["b_resident"] = pick(u[14], [1, 2])
+    if path == 3 and u[16] < 0.5:
+        opts["wide"] = 2
     alpha, beta = (1.0, 0.0)
     if entry != "plain":
         alpha = pick(u[15], [1.0, -0.5, 2.0])

@@ -42,6 +42,9 @@ def _check(cfg, M, N, K):
         assert cfg["ctas"] % 2 == 0                                    # whole clusters of 2
     if cfg["path"] == 2:
         assert M <= 128
+    if cfg["wide"]:
+        units = -(-M // 256) * -(-(-(-N // cfg["bn"])) // 2)
+        assert cfg["path"] == 3 and cfg["ctas"] <= 2 * units and not cfg["b_resident"]
     if cfg["b_resident"]:
         num_n = -(-N // cfg["bn"])
         assert cfg["path"] != 3 and num_n <= 4 and cfg["ctas"] % num_n == 0
@@ -55,7 +58,9 @@ def test_default_plans_fit(binding):
 
 @pytest.mark.parametrize("opts", [dict(path=1), dict(path=3), dict(katoms=1), dict(katoms=2),
                                   dict(epi_warps=4), dict(epi_warps=8), dict(b_resident=1),
-                                  dict(acc_f16=1), dict(b_layout=1), dict(max_ctas=37)])
+                                  dict(acc_f16=1), dict(b_layout=1), dict(max_ctas=37),
+                                  dict(wide=2), dict(wide=2, path=3, epi_warps=8),
+                                  dict(wide=1)])
 def test_forced_plans_fit_or_are_refused(binding, opts):
     accepted = 0
     for M, N, K in _shapes(600, 502 + len(str(opts))):
@@ -74,6 +79,10 @@ def test_forced_plans_fit_or_are_refused(binding, opts):
             assert cfg["epi_warps"] == opts["epi_warps"]
         if "max_ctas" in opts:
             assert cfg["ctas"] <= opts["max_ctas"]
+        if opts.get("wide") == 2:
+            assert cfg["wide"] == 1
+        if opts.get("wide") == 1:
+            assert cfg["wide"] == 0
         if opts.get("b_resident") == 1:
             assert cfg["b_resident"] == 0
         if opts.get("b_layout") == 1:

@@ -5,11 +5,15 @@
 // one thread of the even CTA issues tcgen05.mma.cta_group::2 with M = 256,
 // which reads A from each CTA's shared memory and the two halves of B from
 // both, and accumulates each CTA's 128 x BN block of D in that CTA's TMEM.
-// Per SM, a k-block then costs 16 KiB of A + BN/2 x 128 B of B for
+// Per SM, a 64-wide K slice then costs 16 KiB of A + BN/2 x 128 B of B for
 // 128 x BN x 64 MACs -- half the B bytes of a single-CTA tile of the same
-// width -- so a stage is 32 KiB at BN = 256 and six stages fit, which covers
-// the copy latency measured with all SMs loading (S_min = ceil(T_copy /
-// T_compute) + 1 of "第 6 课：Shared Memory 布局与异步流水", section 4).
+// width.  The ring depth follows S_min = ceil(T_copy / T_compute) + 1 of
+// "第 6 课：Shared Memory 布局与异步流水", section 4, with both latencies
+// measured on the GPU with every SM loading: at BN = 256 the narrow tile
+// holds three stages of two slices (64 KiB each), and the wide unit below
+// four stages of one slice carrying both tiles' B halves (48 KiB each),
+// which is S_min for its measured T_copy (about 2550 cycles from HBM)
+// against T_compute (about 1030 cycles for the slice's MMAs on both tiles).
 //
 // Barriers (same shared-memory offsets in both CTAs):
 //   full[s]      even CTA only, count 1: the even CTA's producer arrives

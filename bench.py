@@ -67,11 +67,37 @@ KERNEL_SOURCES = ("ptx.cuh", "pipeline.cuh", "gemm_kernel.cuh", "gemm_pair_kerne
                   "gemm_tn_f16.cu")
 
 
+def code_tokens(text: str) -> str:
+    """C/C++ source with comments removed and whitespace runs collapsed, so
+    that an edit to comments or layout alone keeps the recorded traffic."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":                       # string or character literal, kept whole
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def source_hash() -> str:
     h = hashlib.sha256()
     for name in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "multistage_smem_pipeline_gb300", "csrc", name), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "multistage_smem_pipeline_gb300", "csrc", name),
+                  encoding="utf-8") as fh:
+            h.update(code_tokens(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

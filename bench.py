@@ -641,8 +641,9 @@ def run_gpu(args, tag):
             iso["frac_of_burst_peak"] = iso["tflops_clean_flush"] / float(peaks["bf16_tflops"])
     direct_d = padded and spec["N"] % 8 != 0     # a padded call with unaligned D rows, C not read
     flag = lambda x: "true" if x else "false"
-    roof["kernel"] = ("gemm_tn_f16_pair<%d, %s, %d>" % (cfg["epi_warps"], flag(direct_d),
-                                                        2 if cfg["wide"] else 1)
+    roof["kernel"] = ("gemm_tn_f16_pair<%d, %s, %d, %s>" % (cfg["epi_warps"], flag(direct_d),
+                                                            2 if cfg["wide"] else 1,
+                                                            flag(scaled))
                       if cfg["path"] == 3 else
                       "gemm_tn_f16_persistent<%d, %s, %s>" % (cfg["epi_warps"],
                                                               flag(cfg["b_resident"]),

@@ -307,11 +307,15 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
           if (lane == 0) mbar_arrive(tempty_bar(acc));
         }
         if (p.acc_f16) widen_f16_accumulator(r);
-        if (p.scaled) apply_alpha_beta(r, p, m0 + lane, n0 + c * kEpiCols);
         const uint32_t buf = my_bufs + (chunk_seq % kEpiBufs) * kEpiChunkBytes;
         if (chunk_seq >= static_cast<uint32_t>(kEpiBufs)) {
           if (lane == 0) bulk_wait_group_read<kEpiBufs - 1>();  // buffer's last store has read it
           __syncwarp();
+        }
+        if (p.scaled) {  // C passes through the staging buffer on its way to the rows' lanes
+          const bool with_c = p.beta != 0.0f;
+          if (with_c) stage_c_chunk(p, m0, n0 + c * kEpiCols, lane, buf);
+          apply_alpha_beta(r, p, with_c, buf, lane);
         }
         // Row `lane` of the 32 x 32 box, 64 bytes = four 16-byte pieces, placed
         // with the 64-byte swizzle the TMA store expects (piece j of row r at

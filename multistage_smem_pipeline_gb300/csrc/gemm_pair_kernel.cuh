@@ -38,6 +38,9 @@
 namespace gb300 {
 
 // kDirectD: as in gemm_tn_f16_persistent.
+// kScaled: the epilogue forms alpha * acc + beta * C (p.scaled); the plain
+// GEMM's instantiation carries none of that code, so its epilogue keeps the
+// registers.
 // kNT: n-tiles per work unit.  With 2 (the "wide" unit), one unit is the
 // 256 x 2*BN block of two adjacent n-tiles: every ring stage carries the A
 // slice once and both tiles' B halves, the MMA thread issues both tiles'
@@ -49,7 +52,7 @@ namespace gb300 {
 // accumulators are no longer double-buffered across units: the next unit's
 // MMAs wait until both are drained.  Each accumulator sees the same MMAs in
 // the same order as with kNT = 1, so the results are bit-identical.
-template <int kEpiWarps, bool kDirectD, int kNT>
+template <int kEpiWarps, bool kDirectD, int kNT, bool kScaled>
 __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
     gemm_tn_f16_pair(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB,
@@ -281,11 +284,15 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
             const int c = c0 + b * kChunkStride;
             if (c > last_c) break;
             if (p.acc_f16) widen_f16_accumulator(r[b]);
-            if (p.scaled) apply_alpha_beta(r[b], p, m0 + lane, n0 + c * kEpiCols);
             const uint32_t buf = my_bufs + (chunk_seq % kEpiBufs) * kEpiChunkBytes;
             if (chunk_seq >= static_cast<uint32_t>(kEpiBufs)) {
               if (lane == 0) bulk_wait_group_read<kEpiBufs - 1>();
               __syncwarp();
+            }
+            if (kScaled) {  // C passes through the staging buffer on its way to the rows' lanes
+              const bool with_c = p.beta != 0.0f;
+              if (with_c) stage_c_chunk(p, m0, n0 + c * kEpiCols, lane, buf);
+              apply_alpha_beta(r[b], p, with_c, buf, lane);
             }
             const uint32_t row_addr = buf + lane * 64u;
             const uint32_t sw = (lane >> 1) & 3u;

@@ -338,23 +338,36 @@ bool grant_smem(Kernel k) {
 
 // Every kernel instantiation: epilogue warps (4, 8) x resident B x direct D
 // store for the single-CTA kernel, epilogue warps x direct D x tiles per unit
-// for the pair.
+// x scaled epilogue for the pair.
 template <bool kDirectD>
 bool grant_all(bool ok) {
   return ok && grant_smem(gemm_tn_f16_persistent<4, false, kDirectD>) &&
          grant_smem(gemm_tn_f16_persistent<8, false, kDirectD>) &&
          grant_smem(gemm_tn_f16_persistent<4, true, kDirectD>) &&
          grant_smem(gemm_tn_f16_persistent<8, true, kDirectD>) &&
-         grant_smem(gemm_tn_f16_pair<4, kDirectD, 1>) &&
-         grant_smem(gemm_tn_f16_pair<8, kDirectD, 1>) &&
-         grant_smem(gemm_tn_f16_pair<4, kDirectD, 2>) && grant_smem(gemm_tn_f16_pair<8, kDirectD, 2>);
+         grant_smem(gemm_tn_f16_pair<4, kDirectD, 1, false>) &&
+         grant_smem(gemm_tn_f16_pair<8, kDirectD, 1, false>) &&
+         grant_smem(gemm_tn_f16_pair<4, kDirectD, 2, false>) &&
+         grant_smem(gemm_tn_f16_pair<8, kDirectD, 2, false>) &&
+         grant_smem(gemm_tn_f16_pair<4, kDirectD, 1, true>) &&
+         grant_smem(gemm_tn_f16_pair<8, kDirectD, 1, true>) &&
+         grant_smem(gemm_tn_f16_pair<4, kDirectD, 2, true>) &&
+         grant_smem(gemm_tn_f16_pair<8, kDirectD, 2, true>);
+}
+
+template <bool kDirectD, int kNT, bool kScaled>
+cudaError_t launch_pair_as(const cudaLaunchConfig_t& cfg, int epi_warps, const CUtensorMap& a,
+                           const CUtensorMap& b, const CUtensorMap& d, const GemmParams& p) {
+  return epi_warps == 8
+             ? cudaLaunchKernelEx(&cfg, gemm_tn_f16_pair<8, kDirectD, kNT, kScaled>, a, b, d, p)
+             : cudaLaunchKernelEx(&cfg, gemm_tn_f16_pair<4, kDirectD, kNT, kScaled>, a, b, d, p);
 }
 
 template <bool kDirectD, int kNT>
 cudaError_t launch_pair(const cudaLaunchConfig_t& cfg, int epi_warps, const CUtensorMap& a,
                         const CUtensorMap& b, const CUtensorMap& d, const GemmParams& p) {
-  return epi_warps == 8 ? cudaLaunchKernelEx(&cfg, gemm_tn_f16_pair<8, kDirectD, kNT>, a, b, d, p)
-                        : cudaLaunchKernelEx(&cfg, gemm_tn_f16_pair<4, kDirectD, kNT>, a, b, d, p);
+  return p.scaled ? launch_pair_as<kDirectD, kNT, true>(cfg, epi_warps, a, b, d, p)
+                  : launch_pair_as<kDirectD, kNT, false>(cfg, epi_warps, a, b, d, p);
 }
 
 template <bool kDirectD>
@@ -398,7 +411,7 @@ int prepare_device(DeviceState* st) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&clusters, gemm_tn_f16_pair<8, false, 1>, &cfg) !=
+  if (cudaOccupancyMaxActiveClusters(&clusters, gemm_tn_f16_pair<8, false, 1, false>, &cfg) !=
           cudaSuccess ||
       clusters < 1) {
     cudaGetLastError();

@@ -130,33 +130,6 @@ __device__ __forceinline__ void widen_f16_accumulator(uint32_t (&r)[32]) {
     r[i] = __float_as_uint(__half2float(__ushort_as_half(static_cast<unsigned short>(r[i]))));
 }
 
-// r (fp32 bits of one row's 32 accumulator columns) <- alpha * r + beta * C
-// for row `row`, columns [col, col + 32) of C.  Groups of 8 columns that
-// start at or past N, and rows past M, are not read; a group that straddles N
-// reads up to the next multiple of 8, which the row stride ldc covers.
-__device__ __forceinline__ void apply_alpha_beta(uint32_t (&r)[32], const GemmParams& p, int row,
-                                                 int col) {
-#pragma unroll
-  for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(p.alpha * __uint_as_float(r[i]));
-  if (p.beta == 0.0f || row >= p.M) return;
-  const uint16_t* c_row = p.C + static_cast<size_t>(row) * p.ldc + col;
-#pragma unroll
-  for (int g = 0; g < 4; ++g) {
-    if (col + 8 * g < p.N) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(c_row + 8 * g));
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const __half2 h = *reinterpret_cast<const __half2*>(&w[q]);
-        const float2 f = __half22float2(h);
-        r[8 * g + 2 * q] = __float_as_uint(fmaf(p.beta, f.x, __uint_as_float(r[8 * g + 2 * q])));
-        r[8 * g + 2 * q + 1] =
-            __float_as_uint(fmaf(p.beta, f.y, __uint_as_float(r[8 * g + 2 * q + 1])));
-      }
-    }
-  }
-}
-
 __device__ __forceinline__ uint16_t ld_shared_u16(uint32_t addr) {
   uint16_t v;
   asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
@@ -188,6 +161,67 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
                "r"(d)
                : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// The C term of the scaled epilogue for the warp's 32 x 32 chunk (rows
+// [m0, m0 + 32), columns [col, col + 32)), copied into the warp's staging
+// buffer `buf` (free to overwrite) with cp.async, in the layout of the
+// epilogue's stores: 16-byte piece j of row r at j ^ ((r >> 1) & 3).  Copy i
+// of a lane is row 8 i + lane / 4, piece lane % 4, so one warp-wide copy
+// reads 64 contiguous bytes of each of 8 rows -- 8 whole lines of C, where
+// one row per lane would touch 32 lines for 16 bytes each -- and no register
+// holds C on the way.  Rows at or past M and pieces at or past N are
+// zero-filled without reading C (nothing is stored there); a piece that
+// straddles N reads up to the next multiple of 8, which the row stride ldc
+// covers.  Returns once the chunk is in `buf` and visible to the warp.
+__device__ __forceinline__ void stage_c_chunk(const GemmParams& p, int m0, int col, int lane,
+                                              uint32_t buf) {
+  const uint32_t piece = static_cast<uint32_t>(lane) & 3u;
+  const int c8 = col + 8 * static_cast<int>(piece);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t r = 8u * i + (static_cast<uint32_t>(lane) >> 2);
+    const int row = m0 + static_cast<int>(r);
+    const bool in = row < p.M && c8 < p.N;
+    const uint16_t* src = in ? p.C + static_cast<size_t>(row) * p.ldc + c8 : p.C;
+    cp_async_16(buf + r * 64u + ((piece ^ ((r >> 1) & 3u)) << 4), src, in ? 16u : 0u);
+  }
+  cp_async_wait_all();
+  __syncwarp();
+}
+
+// r (fp32 bits of row `lane` of the chunk) <- alpha * r, then + beta * C when
+// stage_c_chunk has put the chunk's C in `buf`: each lane reads back its own
+// row, the only row it later writes, so `buf` can then take the row's D
+// values without another barrier.
+__device__ __forceinline__ void apply_alpha_beta(uint32_t (&r)[32], const GemmParams& p,
+                                                 bool with_c, uint32_t buf, int lane) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(p.alpha * __uint_as_float(r[i]));
+  if (!with_c) return;
+  const uint32_t sw = (static_cast<uint32_t>(lane) >> 1) & 3u;
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    const uint4 c = ld_shared_v4(buf + static_cast<uint32_t>(lane) * 64u + ((g ^ sw) << 4));
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const __half2 h = *reinterpret_cast<const __half2*>(&w[q]);
+      const float2 f = __half22float2(h);
+      r[8 * g + 2 * q] = __float_as_uint(fmaf(p.beta, f.x, __uint_as_float(r[8 * g + 2 * q])));
+      r[8 * g + 2 * q + 1] =
+          __float_as_uint(fmaf(p.beta, f.y, __uint_as_float(r[8 * g + 2 * q + 1])));
+    }
+  }
 }
 
 }  // namespace gb300

@@ -400,7 +400,8 @@ def run_gpu(args, tag):
             "epi_warps": args.epi_warps, "b_resident": args.b_resident, "pdl": args.pdl,
             "wide": args.wide}
     forced = any(opts.values())
-    cfg = binding.query_config(M, N, K, b_layout=1 if spec.get("b_kn") else 0, **opts)
+    cfg = binding.query_config(M, N, K, b_layout=1 if spec.get("b_kn") else 0,
+                               acc_f16=1 if spec.get("acc_f16") else 0, **opts)
 
     # Operand copies for the timed launches: launch i uses copy i % R, and the R
     # copies together span at least 3 x L2, so every launch reads operands that

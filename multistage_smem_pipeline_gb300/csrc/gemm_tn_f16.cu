@@ -263,21 +263,26 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   if (fit < 2) return GEMM_ERR_INVALID_VALUE;
   const int stages = o.kstage ? o.kstage : fit;
   if (stages > fit) return GEMM_ERR_INVALID_VALUE;
+  // Balanced grids: as many CTAs (pairs) as the fewest waves need, so every
+  // one gets the same number of tiles (units) to one.  An HBM-bound stream
+  // then has no partial last wave (tall 81920 x 256 x 256: 640 tiles as 5 on
+  // each of 128 CTAs instead of 4 or 5 on 152, 18.6 against 18.9 us); on the
+  // tensor-bound pair path the idle SMs leave the busy ones more of the power
+  // cap (4096^3: 128 units as 2 on 64 pairs, 85.1 against 85.5 us).
+  const auto balanced = [](int64_t work, int64_t slots, int64_t multiple) {
+    const int64_t waves = (work + slots - 1) / slots;
+    const int64_t even = (work + waves - 1) / waves;
+    return std::min<int64_t>(slots, (even + multiple - 1) / multiple * multiple);
+  };
   int ctas;
   if (path == GEMM_PATH_PAIR) {
     int64_t pairs = std::min<int64_t>(units, max_pairs);
     if (o.max_ctas) pairs = std::min<int64_t>(pairs, std::max(1, o.max_ctas / 2));
-    ctas = static_cast<int>(2 * pairs);
+    ctas = static_cast<int>(2 * balanced(units, pairs, 1));
   } else if (b_resident) {
-    // Every CTA gets the same number of tiles (to one): as many CTAs as the
-    // fewest waves need, a multiple of num_n.  An HBM-bound stream then has
-    // no partial last wave (tall 81920 x 256 x 256: 640 tiles as 5 on each
-    // of 128 CTAs instead of 4 or 5 on 152, 18.6 against 18.9 us).
-    const int64_t waves = (tiles + ctas_res - 1) / ctas_res;
-    const int64_t even = (tiles + waves - 1) / waves;
-    ctas = static_cast<int>(std::min<int64_t>(ctas_res, (even + num_n - 1) / num_n * num_n));
+    ctas = static_cast<int>(balanced(tiles, ctas_res, num_n));  // a multiple of num_n
   } else {
-    ctas = static_cast<int>(ctas_1);
+    ctas = static_cast<int>(balanced(tiles, ctas_1, 1));
   }
   const int group_m =
       o.group_m ? o.group_m

@@ -227,26 +227,16 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
                             ctas_res >= 1 && (num_n == 1 || o.group_m <= 1);
   if (o.b_resident == 2 && !res_possible) return GEMM_ERR_INVALID_VALUE;
   if (res_possible && (o.b_resident == 2 || (o.b_resident == 0 && tiles >= 2 * sms))) {
-    // The streamed A is the whole of the HBM traffic here, so take the
-    // carve-up with the most A bytes in flight: with B resident, four
-    // epilogue warps can leave room for one more A stage than eight (tall
-    // 81920 x 256 x 256: 3, 4 and 5 stages measured 20.5, 19.1 and 18.4 us).
-    // Ties keep the first candidate (the default epilogue width, 2 slices).
-    // Not with the fp16 accumulator, whose widening step makes four warps
-    // the slower side (the same shape: 19.6 against 18.7 us).
     const int min_stages = (o.b_resident == 2) ? 2 : 3;
-    int best_inflight = 0;
     for (int ew : {epi_warps, 4}) {
-      if (o.epi_warps && ew != o.epi_warps) continue;
-      if (!o.epi_warps && o.acc_f16 && ew != epi_warps && best_inflight > 0) continue;
+      if (b_resident || (o.epi_warps && ew != o.epi_warps)) continue;
       for (int ka : {2, 1}) {
-        if (o.katoms && ka != o.katoms) continue;
+        if (b_resident || (o.katoms && ka != o.katoms)) continue;
         const uint32_t bres = static_cast<uint32_t>((K + kBK * ka - 1) / (kBK * ka)) * ka *
                               b_atom_bytes_for(path, bn);
         if (bres > static_cast<uint32_t>(kMaxDynSmem)) continue;
         const int f = stages_that_fit(static_cast<uint32_t>(ka) * kABytes, ew, bres);
-        if (f >= min_stages && (ka == 1 || o.katoms || f >= 3) && f * ka > best_inflight) {
-          best_inflight = f * ka;
+        if (f >= min_stages && (ka == 1 || o.katoms || f >= 3)) {
           b_resident = true;
           bres_bytes = bres;
           epi_warps = ew;
@@ -266,9 +256,10 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   // Balanced grids: as many CTAs (pairs) as the fewest waves need, so every
   // one gets the same number of tiles (units) to one.  An HBM-bound stream
   // then has no partial last wave (tall 81920 x 256 x 256: 640 tiles as 5 on
-  // each of 128 CTAs instead of 4 or 5 on 152, 18.6 against 18.9 us); on the
-  // tensor-bound pair path the idle SMs leave the busy ones more of the power
-  // cap (4096^3: 128 units as 2 on 64 pairs, 85.1 against 85.5 us).
+  // each of 128 CTAs instead of 4 or 5 on 152, 18.6 against 19.0 us back to
+  // back, the same 20.8 us launched alone); on the tensor-bound pair path the
+  // idle SMs leave the busy ones more of the power cap (4096^3: 128 units as
+  // 2 on 64 pairs, 85.1 against 85.5 us).
   const auto balanced = [](int64_t work, int64_t slots, int64_t multiple) {
     const int64_t waves = (work + slots - 1) / slots;
     const int64_t even = (work + waves - 1) / waves;

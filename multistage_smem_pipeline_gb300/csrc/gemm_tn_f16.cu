@@ -256,7 +256,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   // Balanced grids: as many CTAs (pairs) as the fewest waves need, so every
   // one gets the same number of tiles (units) to one.  An HBM-bound stream
   // then has no partial last wave (tall 81920 x 256 x 256: 640 tiles as 5 on
-  // each of 128 CTAs instead of 4 or 5 on 152, 18.6 against 19.0 us back to
+  // each of 128 CTAs instead of 4 or 5 on 152, 18.6 against 18.9 us back to
   // back, the same 20.8 us launched alone); on the tensor-bound pair path the
   // idle SMs leave the busy ones more of the power cap (4096^3: 128 units as
   // 2 on 64 pairs, 85.1 against 85.5 us).

@@ -49,6 +49,17 @@ def _check(cfg, M, N, K):
         num_n = -(-N // cfg["bn"])
         assert cfg["path"] != 3 and num_n <= 4 and cfg["ctas"] % num_n == 0
         assert num_n == 1 or cfg["group_m"] == 1
+    # balanced grids: with one CTA fewer (one pair fewer; num_n CTAs fewer with
+    # resident B) the same work would need another wave
+    if cfg["path"] == 3:
+        num_n = -(-N // cfg["bn"])
+        work = -(-M // 256) * (-(-num_n // 2) if cfg["wide"] else num_n)
+        slots, step = cfg["ctas"] // 2, 1
+    else:
+        work, slots = cfg["tiles"], cfg["ctas"]
+        step = -(-N // cfg["bn"]) if cfg["b_resident"] else 1
+    waves = -(-work // slots)
+    assert slots - step < 1 or (slots - step) * waves < work, (cfg, work)
 
 
 def test_default_plans_fit(binding):

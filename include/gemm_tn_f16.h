@@ -74,7 +74,9 @@ typedef struct {
   int bn;              /* tile width along N: 0 = choose, else 32..256, % 32 == 0
                           (GEMM_PATH_PAIR: the pair's width; each CTA loads bn/2 rows of B) */
   int kstage;          /* shared-memory ring depth: 0 = deepest that fits, else 2..16 */
-  int max_ctas;        /* persistent CTAs: 0 = one per SM                        */
+  int max_ctas;        /* persistent CTAs at most: 0 = one per SM.  The grid is then
+                          balanced: the fewest CTAs (pairs) that keep the fewest
+                          waves of tiles (units), so each gets the same number to one */
   int group_m;         /* m-blocks per rasterisation group: 0 = choose           */
   uint64_t timeout_ns; /* per-wait limit inside the kernel: 0 = 2 s              */
   int inject;          /* test hook: 1 = the producer announces its first stage

@@ -269,6 +269,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
         // hold up the next unit's MMAs.
         for (int c0 = half; c0 <= last_c && rows_live; c0 += kChunkStride * kEpiBatch) {
           uint32_t r[kEpiBatch][32];
+          bool c_ahead = false;  // the scaled epilogue: this chunk's C was sent ahead
 #pragma unroll
           for (int b = 0; b < kEpiBatch; ++b)
             if (c0 + b * kChunkStride <= last_c)
@@ -285,13 +286,35 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
             if (c > last_c) break;
             if (p.acc_f16) widen_f16_accumulator(r[b]);
             const uint32_t buf = my_bufs + (chunk_seq % kEpiBufs) * kEpiChunkBytes;
-            if (chunk_seq >= static_cast<uint32_t>(kEpiBufs)) {
+            const bool with_c = kScaled && p.beta != 0.0f;
+            if (!(with_c && c_ahead) && chunk_seq >= static_cast<uint32_t>(kEpiBufs)) {
               if (lane == 0) bulk_wait_group_read<kEpiBufs - 1>();
               __syncwarp();
             }
             if (kScaled) {  // C passes through the staging buffer on its way to the rows' lanes
-              const bool with_c = p.beta != 0.0f;
-              if (with_c) stage_c_chunk(p, m0, n0 + c * kEpiCols, lane, buf);
+              if (with_c) {
+                // This chunk's C is already in flight when the previous chunk
+                // of the batch sent it ahead; the next chunk's C goes into the
+                // other buffer once that buffer's last store has read it, and
+                // lands while this chunk is finished.
+                if (!c_ahead) {
+                  copy_c_chunk(p, m0, n0 + c * kEpiCols, lane, buf);
+                  cp_async_commit();
+                }
+                const int cn = c + kChunkStride;
+                c_ahead = b + 1 < kEpiBatch && cn <= last_c;
+                if (c_ahead) {
+                  if (lane == 0) bulk_wait_group_read<0>();
+                  __syncwarp();
+                  copy_c_chunk(p, m0, n0 + cn * kEpiCols, lane,
+                               my_bufs + ((chunk_seq + 1) % kEpiBufs) * kEpiChunkBytes);
+                  cp_async_commit();
+                  cp_async_wait_pending<1>();
+                } else {
+                  cp_async_wait_pending<0>();
+                }
+                __syncwarp();
+              }
               apply_alpha_beta(r[b], p, with_c, buf, lane);
             }
             const uint32_t row_addr = buf + lane * 64u;

@@ -183,8 +183,10 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
 // zero-filled without reading C (nothing is stored there); a piece that
 // straddles N reads up to the next multiple of 8, which the row stride ldc
 // covers.  Returns once the chunk is in `buf` and visible to the warp.
-__device__ __forceinline__ void stage_c_chunk(const GemmParams& p, int m0, int col, int lane,
-                                              uint32_t buf) {
+// The copies alone, not committed: the caller commits and waits (the pair
+// kernel's epilogue keeps the next chunk's copies in flight this way).
+__device__ __forceinline__ void copy_c_chunk(const GemmParams& p, int m0, int col, int lane,
+                                             uint32_t buf) {
   const uint32_t piece = static_cast<uint32_t>(lane) & 3u;
   const int c8 = col + 8 * static_cast<int>(piece);
 #pragma unroll
@@ -195,6 +197,11 @@ __device__ __forceinline__ void stage_c_chunk(const GemmParams& p, int m0, int c
     const uint16_t* src = in ? p.C + static_cast<size_t>(row) * p.ldc + c8 : p.C;
     cp_async_16(buf + r * 64u + ((piece ^ ((r >> 1) & 3u)) << 4), src, in ? 16u : 0u);
   }
+}
+
+__device__ __forceinline__ void stage_c_chunk(const GemmParams& p, int m0, int col, int lane,
+                                              uint32_t buf) {
+  copy_c_chunk(p, m0, col, lane, buf);
   cp_async_wait_all();
   __syncwarp();
 }

@@ -535,6 +535,8 @@ def run_gpu(args, tag):
         iso_dirty = isolated_launches(n_iso, False)
         iso = {"steps": n_iso, "mean_ms_clean_flush": statistics.mean(iso_clean),
                "median_ms_clean_flush": statistics.median(iso_clean),
+               "p10_ms_clean_flush": float(np.percentile(iso_clean, 10)),
+               "p90_ms_clean_flush": float(np.percentile(iso_clean, 90)),
                "mean_ms_write_only_flush": statistics.mean(iso_dirty),
                "note": "per-launch event pairs after an L2 flush; includes the isolated "
                        "launch latency (an empty kernel measures ~4.5 us this way)"}

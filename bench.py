@@ -216,6 +216,22 @@ def oracle_rate(tag, a_bits, b_bits, target_s: float):
     return 2.0 * rows * N * K / dt, rows, min(threads, rows), dt
 
 
+def oracle_rate_one_thread(tag, a_bits, b_bits, target_s: float):
+    """The same oracle on one thread, over as many rows as fit in about
+    target_s seconds.  Returns (flop/s, rows, seconds)."""
+    spec = synthetic.WORKLOADS[tag]
+    K, N = spec["K"], spec["N"]
+    t0 = time.perf_counter()
+    oracle_block(tag, a_bits, b_bits, 1, N, 1)()
+    one_row = max(time.perf_counter() - t0, 1e-6)
+    rows = int(max(1, min(spec["M"], round(target_s / one_row))))
+    step = oracle_block(tag, a_bits, b_bits, rows, N, 1)
+    t0 = time.perf_counter()
+    step()
+    dt = time.perf_counter() - t0
+    return 2.0 * rows * N * K / dt, rows, dt
+
+
 def oracle_kind(spec) -> str:
     if spec.get("acc_f16"):
         return "oracle with an fp16 accumulator rounded after every 16-deep K slice"
@@ -698,10 +714,14 @@ def run_gpu(args, tag):
             "wall_s_timed_region": wall}
     if world == 1 and not args.no_cpu:
         rate, rows, cores, dt = oracle_rate(tag, a_bits, b_bits, args.cpu_seconds)
+        rate1, rows1, dt1 = oracle_rate_one_thread(tag, a_bits, b_bits,
+                                                   min(2.0, args.cpu_seconds / 4))
         line["cpu_baseline"] = {"value": rate / 1e12, "unit": UNIT, "cores": cores,
                                 "kind": "oracle",
                                 "sample": f"{rows} rows of D ({rows}x{N}, K={K}) in {dt:.1f} s; "
-                                          f"{oracle_kind(spec)}"}
+                                          f"{oracle_kind(spec)}",
+                                "one_thread": {"value": rate1 / 1e12, "unit": UNIT, "cores": 1,
+                                               "sample": f"{rows1} rows of D in {dt1:.2f} s"}}
     print(json.dumps(line))
     return 0
 

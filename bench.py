@@ -721,7 +721,8 @@ def run_gpu(args, tag):
                                 "sample": f"{rows} rows of D ({rows}x{N}, K={K}) in {dt:.1f} s; "
                                           f"{oracle_kind(spec)}",
                                 "one_thread": {"value": rate1 / 1e12, "unit": UNIT, "cores": 1,
-                                               "sample": f"{rows1} rows of D in {dt1:.2f} s"}}
+                                               "sample": f"{rows1} rows of D in {dt1:.2f} s"},
+                                "full_problem_s_extrapolated": flops / rate}
     print(json.dumps(line))
     return 0
 

@@ -10,13 +10,24 @@ launch reads operands evicted from L2 by the launches in between (inputs
 larger than L2); ms_per_step = elapsed / K.  Default workload: 8192 x 8192 x
 8192, U[-1, 1] operands.
 
-Extra keys: roofline (the GEMM kernel against the measured dense bf16 peak,
-fp16 running at the same nominal rate, or against measured HBM bandwidth for
-the skinny case), launch_ms_isolated (the same launch timed alone after an
-L2 flush, per-launch events: adds the isolated-launch latency), cpu_baseline
-(the CPU oracle timed on a bounded row slice of the same workload on this
-host), e2e (host buffers: H2D of A and B, the GEMM, D2H of D, per step),
-clocks (nvidia-smi sampled during the timed region), gpu_launches.
+Extra keys:
+  roofline         the GEMM kernel against the measured peak that binds: HBM
+                   copy bandwidth when the arithmetic intensity is under the
+                   measured ridge point, else the dense bf16 tensor rate (fp16
+                   runs at the same nominal rate) -- the burst figure when the
+                   timed region lasts under a second, the sustained (power-
+                   capped) figure when it lasts longer;
+  tensor_nominal   the same rate against SMs x 8192 flop/clk x SM clock, at the
+                   maximum clock and at the clock sampled in the timed region;
+  sustained        the same launches back to back for --sustained-s seconds:
+                   the power-capped rate, with its own clock record;
+  configs          (default workload) the other configurations -- 256^3,
+                   1024^3 {-1,0,1}, 4096^3, the skinny 128 x 14336 x 4096 and the
+                   tall 81920 x 256 x 256 -- each timed back to back with its
+                   roofline, its D checked against the oracle (max |err|, ulps,
+                   exact fraction) and the oracle's CPU rate on that check;
+  launch_ms_isolated, cpu_baseline, e2e, clocks (NVML sampled every 5 ms
+  during the timed region), gpu_launches.
 
 --impl reference times the CPU oracle itself (the only other implementation
 of this computation here) on the same workload and metric.
@@ -119,59 +130,157 @@ def recorded_traffic(workload: str):
 CLOCK_FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
                 "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
                 "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+# NVML clock-event reason bits (nvmlClocksEventReason*), the ones a run is judged by
+REASON_BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+               "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80}
+NVML_CLOCK_SM = 1
+
+
+def reasons_from_mask(mask: int) -> list:
+    return sorted(n for n, bit in REASON_BITS.items() if mask & bit)
+
+
+class _Nvml:
+    """The few NVML queries the sampler needs, through ctypes (read-only:
+    current and maximum SM clock, power draw, clock-event reasons)."""
+
+    def __init__(self, bus_id: str):
+        import ctypes
+        self.c = ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit_v2 failed")
+        self.lib = lib
+        self.h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByPciBusId_v2(bus_id.encode(), ctypes.byref(self.h)) != 0:
+            raise OSError(f"no NVML device at {bus_id}")
+        self._reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        mx = ctypes.c_uint(0)
+        lib.nvmlDeviceGetMaxClockInfo(self.h, NVML_CLOCK_SM, ctypes.byref(mx))
+        self.max_mhz = float(mx.value)
+
+    def sample(self):
+        c = self.c
+        clk, pw, rs = c.c_uint(0), c.c_uint(0), c.c_ulonglong(0)
+        if self.lib.nvmlDeviceGetClockInfo(self.h, NVML_CLOCK_SM, c.byref(clk)) != 0:
+            return None
+        self.lib.nvmlDeviceGetPowerUsage(self.h, c.byref(pw))
+        self._reasons(self.h, c.byref(rs))
+        return float(clk.value), pw.value / 1000.0, int(rs.value)
 
 
 class ClockSampler:
-    def __init__(self, index: int):
-        self.index = index
-        self.proc = None
-        self.lines = []
+    """SM clock, power draw and clock-event reasons of one GPU, sampled every
+    `period_s` on a background thread, each sample stamped with the host's
+    perf_counter so a region's samples can be picked out afterwards.  NVML
+    through ctypes (5 ms period by default); nvidia-smi -lms where NVML
+    cannot be loaded.  The GPU is named by its PCI bus id, so the samples
+    describe the device this process computes on whatever
+    CUDA_VISIBLE_DEVICES says."""
+
+    def __init__(self, bus_id: str, period_s: float = 0.005):
+        self.bus_id = bus_id
+        self.period_s = period_s
+        self.samples = []          # (t, sm_mhz, power_w, reason mask)
+        self.max_mhz = None
+        self.source = None
+        self._stop = threading.Event()
         self._t = None
+        self.proc = None
 
     def start(self):
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + ",".join(CLOCK_FIELDS),
-                 "--format=csv,noheader,nounits", "-lms", "50"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self._t = threading.Thread(target=self._read, daemon=True)
-            self._t.start()
-            time.sleep(0.3)
-        except OSError:
-            self.proc = None
+            nv = _Nvml(self.bus_id)
+            self.max_mhz = nv.max_mhz
+            self.source = f"NVML every {self.period_s * 1e3:.0f} ms"
+            self._t = threading.Thread(target=self._poll, args=(nv,), daemon=True)
+        except (OSError, AttributeError):
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", self.bus_id, "--query-gpu=" + ",".join(CLOCK_FIELDS),
+                     "--format=csv,noheader,nounits", "-lms", "10"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except OSError:
+                return
+            self.source = "nvidia-smi -lms 10"
+            self._t = threading.Thread(target=self._read_smi, daemon=True)
+        self._t.start()
+        time.sleep(0.05)
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
+    def _poll(self, nv):
+        while not self._stop.is_set():
+            s = nv.sample()
+            if s is not None:
+                self.samples.append((time.perf_counter(),) + s)
+            time.sleep(self.period_s)
 
-    def stop(self):
-        if not self.proc:
-            return None
-        time.sleep(0.1)
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        self._t.join(timeout=5)
-        sm, mx, reasons = [], [], set()
+    def _read_smi(self):
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        for line in self.proc.stdout:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) != len(CLOCK_FIELDS):
                 continue
             try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
+                sm, mx = float(parts[0]), float(parts[1])
+                pw = float(parts[2])
             except ValueError:
                 continue
-            for n, v in zip(names, parts[4:]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
+            self.max_mhz = mx
+            mask = sum(REASON_BITS[n] for n, v in zip(names, parts[4:])
+                       if v.lower().startswith("active"))
+            self.samples.append((time.perf_counter(), sm, pw, mask))
+
+    def stop(self):
+        self._stop.set()
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self._t:
+            self._t.join(timeout=5)
+
+    def region(self, t0: float, t1: float):
+        """Summary of the samples taken between host times t0 and t1; when
+        none fell inside (a region shorter than the period), the nearest one."""
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        if not inside and self.samples:
+            mid = 0.5 * (t0 + t1)
+            inside = [min(self.samples, key=lambda s: abs(s[0] - mid))]
+        if not inside:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+        sm = [s[1] for s in inside]
+        mask = 0
+        for s in inside:
+            mask |= s[3]
+        return {"sm_mhz": statistics.median(sm), "sm_mhz_min": min(sm),
+                "sm_max_mhz": self.max_mhz, "power_w_max": max(s[2] for s in inside),
+                "samples": len(inside), "reasons": reasons_from_mask(mask),
+                "source": self.source}
+
+
+def pci_bus_id(torch, dev) -> str:
+    p = torch.cuda.get_device_properties(dev)
+    return f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+
+
+# The dense fp16 rate of one SM's tensor pipe: a 128 x 256 x 16 kind::f16
+# MMA (1,048,576 flops) every 128 cycles; the MMA latency probe of this
+# library measures 513 cycles for four of them (8176 flop/clk).
+TENSOR_FLOP_PER_CLK_PER_SM = 8192
+
+
+def tensor_nominal(tflops: float, sms: int, max_mhz, sm_mhz) -> dict:
+    """The fraction of the nominal dense tensor rate (SMs x flop/clk x clock),
+    at the maximum SM clock and at the clock sampled under load."""
+    out = {"flop_per_clk_per_sm": TENSOR_FLOP_PER_CLK_PER_SM, "sms": sms}
+    for key, mhz in (("max_clock", max_mhz), ("sampled_clock", sm_mhz)):
+        if mhz:
+            peak = sms * TENSOR_FLOP_PER_CLK_PER_SM * mhz * 1e6 / 1e12
+            out[key] = {"sm_mhz": mhz, "peak_tflops": peak, "frac": tflops / peak}
+    return out
 
 
 # ------------------------------------------------------------------ CPU oracle
@@ -230,6 +339,33 @@ def oracle_rate_one_thread(tag, a_bits, b_bits, target_s: float):
     step()
     dt = time.perf_counter() - t0
     return 2.0 * rows * N * K / dt, rows, dt
+
+
+def fp16_order(bits: np.ndarray) -> np.ndarray:
+    """fp16 bit patterns as integers in the order of their values (+0 == -0),
+    so that the difference of two is their distance in fp16 ulps."""
+    b = bits.astype(np.int64)
+    mag = b & 0x7FFF
+    return np.where(b & 0x8000, -mag, mag)
+
+
+def parity_stats(got: np.ndarray, ref: np.ndarray, K: int, amax: float, bmax: float) -> dict:
+    """Element-wise agreement of the GPU's D with the oracle's on the same
+    elements, against the bound |d - ref| <= 2e-3 sqrt(K) max|A| max|B| +
+    ulp(ref) (fp32 accumulation against exact accumulation, both rounded to
+    fp16 once)."""
+    g = got.view(np.float16).astype(np.float64)
+    r = ref.view(np.float16).astype(np.float64)
+    ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(r), 2.0 ** -14))) - 10)
+    tol = 2e-3 * np.sqrt(max(K, 1)) * amax * bmax + ulp
+    err = np.abs(g - r)
+    err = np.where(np.isnan(g) & np.isnan(r), 0.0, err)
+    err = np.where(np.isnan(err), np.inf, err)
+    ulps = np.abs(fp16_order(got) - fp16_order(ref))
+    return {"elements": int(got.size), "out_of_bound": int(np.count_nonzero(err > tol)),
+            "max_abs_err": float(err.max()), "max_ulps": int(ulps.max()),
+            "exact_frac": float(np.mean(got == ref)), "bit_exact": bool(np.array_equal(got, ref)),
+            "bound": "2e-3*sqrt(K)*max|A|*max|B| + 1 ulp"}
 
 
 def oracle_kind(spec) -> str:
@@ -378,6 +514,131 @@ def padded_gemm_kernel_ms(args, binding, torch, dev, stream, spec, a, b, l2):
     return ms, note
 
 
+# The other configurations of the headline metric's set, measured in the same
+# run: launches timed back to back, and the oracle's check of the result.
+CONFIG_TAGS = ("c1", "c2", "c3", "c5", "c6")
+CONFIG_LAUNCHES = {"c1": 400, "c2": 400, "c3": 100, "c5": 400, "c6": 400}
+FULL_ORACLE = ("c1", "c2")          # checked on every element; the rest on seeded samples
+
+
+def roofline_of(flops, alg_bytes, ms, peaks, peak_src, region_s):
+    """The roofline that binds (arithmetic intensity against the measured
+    ridge point) with the achieved rate against its measured peak.  A
+    tensor-bound region shorter than a second runs before the power cap
+    settles: the burst peak applies; a longer one takes the sustained peak."""
+    ridge = float(peaks["bf16_tflops"]) * 1e12 / (float(peaks["hbm_gbs"]) * 1e9)
+    if flops / alg_bytes < ridge:
+        achieved = alg_bytes / (ms * 1e-3) / 1e9
+        peak = float(peaks["hbm_gbs"])
+        return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "peak_source": f"{peak_src} hbm_gbs (copy bandwidth)"}
+    achieved = flops / (ms * 1e-3) / 1e12
+    burst = float(peaks["bf16_tflops"])
+    sust = float(peaks.get("bf16_tflops_sustained", burst))
+    long_region = region_s >= 1.0
+    peak = sust if long_region else burst
+    key = "bf16_tflops_sustained" if long_region else "bf16_tflops"
+    return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "frac_of_burst_peak": achieved / burst,
+            "frac_of_sustained_peak": achieved / sust,
+            "peak_source": (f"{peak_src} {key}: the timed region lasted {region_s * 1e3:.1f} ms, "
+                            + ("at least 1 s, long enough to reach the power cap"
+                               if long_region else "under 1 s, before the power cap settles")
+                            + "; fp16 runs at the bf16 nominal rate (1:1)")}
+
+
+def time_graph_replays(torch, dev, stream, graph, launches_per_replay, reps, clocks):
+    """Replays `graph` `reps` times back to back between one event pair on
+    `stream`; returns (ms per launch, host window t0, t1, clock summary)."""
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    w0 = time.perf_counter()
+    e0.record(stream)
+    for _ in range(reps):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    w1 = time.perf_counter()
+    ms = e0.elapsed_time(e1) / (reps * launches_per_replay)
+    return ms, w0, w1, (clocks.region(w0, w1) if clocks else None)
+
+
+def bench_config(tag, binding, torch, dev, stream, l2, peaks, peak_src, clocks):
+    """One configuration: ms per launch over back-to-back launches replayed
+    from a CUDA graph and cycling through operand copies that span > 3 x L2,
+    its roofline, and its D checked against the oracle (every element for
+    the small cubes, seeded samples plus tile seams for the rest), the
+    oracle's own time on that check giving its CPU rate."""
+    import oracle
+    spec = synthetic.WORKLOADS[tag]
+    M, N, K = spec["M"], spec["N"], spec["K"]
+    flops = 2.0 * M * N * K
+    alg_bytes = 2.0 * (M * K + N * K + M * N)
+    a_bits, b_bits, _ = synthetic.workload(tag)
+    R = max(2, -(-3 * l2 // int(alg_bytes)))
+    a = torch.from_numpy(a_bits.view(np.float16)).to(dev)
+    b = torch.from_numpy(b_bits.view(np.float16)).to(dev)
+    a_all = a.unsqueeze(0).expand(R, M, K).contiguous()
+    b_all = b.unsqueeze(0).expand(R, N, K).contiguous()
+    d_all = torch.empty((R, M, N), dtype=torch.float16, device=dev)
+    del a, b
+    for i in range(3 * R):
+        binding.gemm_tn_f16(a_all[i % R], b_all[i % R], out=d_all[i % R], stream=stream)
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        cap = torch.cuda.current_stream(dev)
+        for i in range(R):
+            binding.gemm_tn_f16(a_all[i], b_all[i], out=d_all[i], stream=cap)
+    stream.wait_stream(side)
+    g.replay()
+    reps = max(1, CONFIG_LAUNCHES[tag] // R)
+    ms, w0, w1, clk = time_graph_replays(torch, dev, stream, g, R, reps, clocks)
+    status, raw = binding.get_device_error(stream)
+    if status != 0:
+        raise SystemExit(f"device error in the {tag} timing: {raw:#x}")
+    d = d_all[0].cpu().numpy().view(np.uint16)
+    del a_all, b_all, d_all, g
+    cfg = binding.query_config(M, N, K)
+    entry = {"workload": synthetic.WORKLOAD_NAMES[tag], "M": M, "N": N, "K": K,
+             "ms_per_launch": ms, "launches": reps * R,
+             "tflops": flops / (ms * 1e-3) / 1e12, "gbs": alg_bytes / (ms * 1e-3) / 1e9,
+             "roofline": roofline_of(flops, alg_bytes, ms, peaks, peak_src, ms * reps * R / 1e3),
+             "roofline_ms": max(flops / (float(peaks["bf16_tflops"]) * 1e12),
+                                alg_bytes / (float(peaks["hbm_gbs"]) * 1e9)) * 1e3,
+             "plan": {k: cfg[k] for k in ("path", "bn", "kstage", "katoms", "ctas", "epi_warps",
+                                          "b_resident", "wide")},
+             "l2": f"{R} operand copies ({R * int(alg_bytes) >> 20} MiB > 3 x L2) cycled",
+             "clocks": clk}
+    entry["roofline_frac"] = entry["roofline_ms"] / ms
+    # the oracle's check of D, timed: the CPU baseline of this configuration
+    t0 = time.perf_counter()
+    if tag in FULL_ORACLE:
+        threads = oracle.default_threads()
+        ref = oracle.gemm_tn(a_bits, b_bits, threads=threads)
+        got = d
+        sample = f"every element of D ({M} x {N})"
+        o_flops, cores = flops, threads
+    else:
+        rows, cols = synthetic.sample_coords(synthetic.seeds(tag)[2], M, N)
+        ref = oracle.gemm_tn_sampled(a_bits, b_bits, rows, cols)
+        got = d[rows, cols]
+        sample = f"{rows.size} seeded elements of D plus tile seams and corners"
+        o_flops, cores = 2.0 * K * rows.size, 1
+    dt = time.perf_counter() - t0
+    amax = float(np.abs(a_bits.view(np.float16).astype(np.float64)).max())
+    bmax = float(np.abs(b_bits.view(np.float16).astype(np.float64)).max())
+    entry["parity"] = parity_stats(got, ref, K, amax, bmax)
+    entry["parity"]["checked"] = sample
+    entry["parity"]["ok"] = (entry["parity"]["out_of_bound"] == 0 and
+                             (entry["parity"]["bit_exact"] or tag != "c2"))
+    entry["cpu_baseline"] = {"value": o_flops / dt / 1e12, "unit": UNIT, "cores": cores,
+                             "kind": "oracle", "sample": f"{sample} in {dt:.2f} s"}
+    return entry
+
+
 def run_gpu(args, tag):
     import torch
     import torch.distributed as dist
@@ -410,6 +671,7 @@ def run_gpu(args, tag):
         if spec["beta"] != 0:
             alg_bytes += 2.0 * M * N
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
     stream = torch.cuda.current_stream(dev)
     opts = {"path": ["auto", "square", "skinny", "pair"].index(args.path), "bn": args.bn,
             "kstage": args.kstage, "katoms": args.katoms, "group_m": args.group_m,
@@ -512,7 +774,7 @@ def run_gpu(args, tag):
         torch.cuda.synchronize(dev)
         return [x.elapsed_time(y) for x, y in zip(st, en)]
 
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(pci_bus_id(torch, dev), args.clock_period_ms / 1e3)
     clocks.start()
     if world > 1:
         dist.barrier()
@@ -540,10 +802,23 @@ def run_gpu(args, tag):
     else:
         launches_ms = isolated_launches(args.steps, True)
         ms = statistics.mean(launches_ms)
-    wall = time.perf_counter() - wall0
+    wall1 = time.perf_counter()
+    wall = wall1 - wall0
     if world > 1:
         dist.barrier()
-    clk = clocks.stop()
+    clk = clocks.region(wall0, wall1)
+
+    # The same launches for at least --sustained-s seconds back to back: the
+    # power-capped steady state, with its own clock record (the last half of
+    # the window, once the clock has settled).
+    sustained = None
+    if graphs is not None and args.sustained_s > 0:
+        reps = max(1, int(np.ceil(args.sustained_s / (ms * R * 1e-3))))
+        s_ms, w0, w1, _ = time_graph_replays(torch, dev, stream, graphs[0], R, reps, clocks)
+        sustained = {"seconds": s_ms * reps * R / 1e3, "launches": reps * R,
+                     "ms_per_launch": s_ms,
+                     "clocks_whole": clocks.region(w0, w1),
+                     "clocks_steady": clocks.region(w0 + 0.5 * (w1 - w0), w1)}
     iso = None
     if args.alt_steps > 0:
         n_iso = min(args.steps, args.alt_steps)
@@ -627,37 +902,33 @@ def run_gpu(args, tag):
     e2e_ms = slowest_rank_ms(e2e_ms, world)
 
     if rank != 0:
+        clocks.stop()
         return 0
 
     peaks, peak_src = load_peaks()
-    tflops = flops / (ms * 1e-3) / 1e12
     # the dominant kernel's own launch time: the step itself, or for the padded
     # entry the GEMM launch inside it (timed alone on the repacked operands)
     k_ms = kernel_ms if kernel_ms is not None else ms
-    k_tflops = flops / (k_ms * 1e-3) / 1e12
-    # the roofline that binds: arithmetic intensity against the measured ridge point
-    ridge = float(peaks["bf16_tflops"]) * 1e12 / (float(peaks["hbm_gbs"]) * 1e9)
-    hbm_bound = flops / alg_bytes < ridge
-    if hbm_bound:
-        achieved = alg_bytes / (k_ms * 1e-3) / 1e9
-        peak = float(peaks["hbm_gbs"])
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "peak_source": f"{peak_src} hbm_gbs (copy bandwidth)"}
-    else:
-        # back-to-back launches run at the power cap: the sustained peak applies;
-        # a launch timed alone compares with the burst peak
-        sustained = args.timing == "rotate"
-        key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
-        peak = float(peaks.get(key, peaks["bf16_tflops"]))
-        roof = {"bound": "tensor", "achieved": k_tflops, "peak": peak, "unit": "TFLOP/s",
-                "frac": k_tflops / peak,
-                "frac_of_burst_peak": k_tflops / float(peaks["bf16_tflops"]),
-                "peak_source": f"{peak_src} {key} ({'sustained, the timed region is a long run of '
-                               'back-to-back launches' if sustained else 'burst'}) x fp16:bf16 "
-                               f"nominal rate 1:1"}
+    roof = roofline_of(flops, alg_bytes, k_ms, peaks, peak_src, ms * args.steps / 1e3)
+    nominal = None
+    if roof["bound"] == "tensor":
+        nominal = tensor_nominal(roof["achieved"], sms, clk["sm_max_mhz"] if clk else None,
+                                 clk["sm_mhz"] if clk else None)
         if iso:
             iso["tflops_clean_flush"] = flops / (iso["mean_ms_clean_flush"] * 1e-3) / 1e12
             iso["frac_of_burst_peak"] = iso["tflops_clean_flush"] / float(peaks["bf16_tflops"])
+    if sustained is not None:
+        s_roof = roofline_of(flops, alg_bytes, sustained["ms_per_launch"], peaks, peak_src,
+                             sustained["seconds"])
+        sustained["achieved"] = s_roof["achieved"]
+        sustained["unit"] = s_roof["unit"]
+        sustained["frac"] = s_roof["frac"]
+        sustained["peak"] = s_roof["peak"]
+        sustained["peak_source"] = s_roof["peak_source"]
+        st_clk = sustained["clocks_steady"] or sustained["clocks_whole"]
+        if s_roof["bound"] == "tensor" and st_clk:
+            sustained["tensor_nominal"] = tensor_nominal(s_roof["achieved"], sms,
+                                                         st_clk["sm_max_mhz"], st_clk["sm_mhz"])
     direct_d = padded and spec["N"] % 8 != 0     # a padded call with unaligned D rows, C not read
     flag = lambda x: "true" if x else "false"
     roof["kernel"] = ("gemm_tn_f16_pair<%d, %s, %d, %s>" % (cfg["epi_warps"], flag(direct_d),
@@ -702,6 +973,8 @@ def run_gpu(args, tag):
                           if launches_ms else {"mean": ms}),
             "launch_ms_isolated": iso,
             "roofline": roof,
+            "tensor_nominal": nominal,
+            "sustained": sustained,
             "e2e": {"value": job_throughput(flops, world, e2e_ms) / 1e12, "unit": UNIT,
                     "h2d_bytes_per_step": 2 * (M * K + N * K + (M * N if scaled else 0)),
                     "d2h_bytes_per_step": 2 * M * N,
@@ -712,6 +985,12 @@ def run_gpu(args, tag):
             "gpu_launches": args.steps * launches_per_step(spec),
             "clocks": clk,
             "wall_s_timed_region": wall}
+    run_configs = args.configs == "on" or (args.configs == "auto" and tag == "c4")
+    if world == 1 and run_configs:
+        line["configs"] = {t: bench_config(t, binding, torch, dev, stream, l2, peaks, peak_src,
+                                           clocks)
+                           for t in CONFIG_TAGS if t != tag}
+    clocks.stop()
     if world == 1 and not args.no_cpu:
         rate, rows, cores, dt = oracle_rate(tag, a_bits, b_bits, args.cpu_seconds)
         rate1, rows1, dt1 = oracle_rate_one_thread(tag, a_bits, b_bits,
@@ -747,6 +1026,14 @@ def main():
     ap.add_argument("--alt-steps", type=int, default=100,
                     help="extra isolated launches (flush + per-launch events), reported beside "
                          "the value")
+    ap.add_argument("--sustained-s", type=float, default=2.0,
+                    help="seconds of back-to-back launches for the power-capped 'sustained' "
+                         "figure (0 = skip)")
+    ap.add_argument("--configs", choices=["auto", "on", "off"], default="auto",
+                    help="also measure and check the other configurations (auto: with the "
+                         "default 8192^3 workload on one GPU)")
+    ap.add_argument("--clock-period-ms", type=float, default=5.0,
+                    help="clock sampling period during the timed regions")
     ap.add_argument("--katoms", type=int, default=0, help="diagnostics: force K slices per stage")
     ap.add_argument("--group-m", type=int, default=0, help="diagnostics: rasterisation group")
     ap.add_argument("--epi-warps", type=int, default=0, help="diagnostics: epilogue warps (4, 8)")

@@ -13,7 +13,11 @@
  *
  * All entry points are plain C.  Pointers named D, A, B are DEVICE pointers
  * on the current CUDA device; `stream` is a cudaStream_t (NULL = legacy
- * default stream) of that device.  The library allocates no device memory.
+ * default stream) of that device.  No call allocates device memory, with one
+ * exception: the 16 MiB array behind gemm_probe_latencies_static, a static
+ * device array of the library's probe code that a GPU holds from the moment
+ * that code is loaded (at the first use of a probe under lazy module loading,
+ * the CUDA default; at context creation under eager loading) until exit.
  * Every function returns a gemm_status_t value (0 = success) unless stated.
  */
 #ifndef GEMM_TN_F16_H
@@ -247,9 +251,13 @@ int gemm_probe_latencies(int bn, int ctas, const void* scratch, int64_t footprin
  *     footprint_bytes above 16 MiB returns GEMM_ERR_INVALID_VALUE, other
  *     arguments are checked as in gemm_probe_latencies.  16 MiB fits in L2,
  *     so copy_cycles is the L2-resident latency.
- *   - Allocates nothing and calls no allocating routine.  The first call on a
- *     device looks up the array's device address (set-up); make that first
- *     call before any stream capture on the device.
+ *   - Calls no allocating routine.  The first call on a device (and the first
+ *     after the device's context was re-created, e.g. by cudaDeviceReset)
+ *     looks up the array's device address with cudaGetSymbolAddress; under
+ *     lazy module loading, the CUDA default, that lookup may load the
+ *     library's device code and so allocate the 16 MiB array itself.  Make
+ *     that first call early, while 16 MiB are free, and before any stream
+ *     capture on the device; later calls allocate nothing.
  *   - All calls share the array and the result counters (cleared at the start
  *     of each call); calls that overlap on the GPU race and report wrong
  *     numbers.

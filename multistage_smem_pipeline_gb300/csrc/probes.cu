@@ -231,10 +231,16 @@ extern "C" int gemm_probe_latencies(int bn, int ctas, const void* scratch, int64
 // (kStaticProbeScratchBytes) until the process exits.
 //
 // In host code the array's name is only a host-side stand-in for the device
-// symbol, never a device address: the device address is fetched once per
-// device with cudaGetSymbolAddress (with that device current) and cached.
-// That set-up happens in the entry point's first call on each device, so the
-// first call should come before any stream capture on that device.
+// symbol, never a device address.  The device address is fetched with
+// cudaGetSymbolAddress, with the device current, once per device and CUDA
+// context: the cache is keyed on the context's unique id, so a context that
+// was torn down and re-created (cudaDeviceReset) gets a fresh lookup instead
+// of a stale address.  That set-up runs inside the entry point's first call
+// on a device (and its first call after such a reset).  Under lazy module
+// loading, the CUDA default, the lookup may also load this file's device
+// code, and with it allocate the array itself, so make that first call early
+// -- while the device still has 16 MiB free, and before any stream capture
+// on the device.  Later calls allocate nothing.
 //
 // All calls share the array and the probes' result counters.  The array's
 // contents are never relied on (the probe only times loads of it), and the
@@ -249,7 +255,74 @@ constexpr int64_t kStaticProbeScratchBytes = 16ll << 20;  // 16 MiB per device
 static __device__ __align__(256) uint8_t g_probe_static_scratch[kStaticProbeScratchBytes];
 
 std::mutex g_static_mu;
-void* g_static_scratch_ptr[64];  // device address of the array, per device (nullptr = not set up)
+// Device address of the array per device, with the id of the CUDA context it
+// was looked up in (ptr == nullptr: not set up).
+struct StaticScratch {
+  unsigned long long ctx_id;
+  void* ptr;
+};
+StaticScratch g_static_scratch[64];
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+
+// Unique id of the CUDA context current on this thread (driver entry points
+// fetched through the runtime, so nothing links libcuda).  Fails when no
+// context is current yet.  Called with g_static_mu held.
+bool current_context_id(unsigned long long* id) {
+  if (!g_ctx_get_current || !g_ctx_get_id) {
+    void* a = nullptr;
+    void* b = nullptr;
+    cudaDriverEntryPointQueryResult qa, qb;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &qa) !=
+            cudaSuccess ||
+        qa != cudaDriverEntryPointSuccess || !a ||
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) !=
+            cudaSuccess ||
+        qb != cudaDriverEntryPointSuccess || !b) {
+      cudaGetLastError();
+      return false;
+    }
+    g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(a);
+    g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(b);
+  }
+  CUcontext ctx = nullptr;
+  return g_ctx_get_current(&ctx) == CUDA_SUCCESS && ctx != nullptr &&
+         g_ctx_get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// The array's device address on the current device, looked up once per
+// device and context.
+int static_scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= 64) return GEMM_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_static_mu);
+  unsigned long long id = 0;
+  const bool have_id = current_context_id(&id);
+  StaticScratch& e = g_static_scratch[dev];
+  if (have_id && e.ptr && e.ctx_id == id) {
+    *out = e.ptr;
+    return GEMM_OK;
+  }
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_probe_static_scratch) != cudaSuccess || !p) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  // the lookup makes the runtime's context current if none was
+  if (have_id || current_context_id(&id)) {
+    e.ctx_id = id;
+    e.ptr = p;
+  }
+  *out = p;
+  return GEMM_OK;
+}
 
 }  // namespace
 }  // namespace gb300
@@ -259,25 +332,9 @@ extern "C" int gemm_probe_latencies_static(int bn, int ctas, int64_t footprint_b
                                            void* stream) {
   using namespace gb300;
   if (footprint_bytes > kStaticProbeScratchBytes) return GEMM_ERR_INVALID_VALUE;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) {
-    cudaGetLastError();
-    return GEMM_ERR_CUDA;
-  }
-  if (dev < 0 || dev >= 64) return GEMM_ERR_CUDA;
   void* ptr = nullptr;
-  {
-    std::lock_guard<std::mutex> lk(g_static_mu);
-    if (!g_static_scratch_ptr[dev]) {
-      void* p = nullptr;
-      if (cudaGetSymbolAddress(&p, g_probe_static_scratch) != cudaSuccess || !p) {
-        cudaGetLastError();
-        return GEMM_ERR_CUDA;
-      }
-      g_static_scratch_ptr[dev] = p;
-    }
-    ptr = g_static_scratch_ptr[dev];
-  }
+  const int rc = static_scratch_address(&ptr);
+  if (rc != GEMM_OK) return rc;
   // Same probes, same checks (bn, ctas, reps, minimum footprint, device), on
   // the library-owned array instead of a caller-allocated region.
   return gemm_probe_latencies(bn, ctas, ptr, footprint_bytes, reps, copy_cycles, compute_cycles,

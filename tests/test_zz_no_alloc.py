@@ -46,9 +46,16 @@ def _allocating(lib, scratch, footprint, stream):
 def test_static_scratch_probe_matches_allocating_probe(lib, gpu):
     stream = torch.cuda.current_stream(gpu).cuda_stream
     scratch = torch.zeros(FOOTPRINT // 2, dtype=torch.float16, device=gpu)
-    for _ in range(2):                       # two calls in a row share the library's array
+    for call in range(2):                    # two calls in a row share the library's array
+        free_before = torch.cuda.mem_get_info(gpu)[0]
         rc, got = _static(lib, FOOTPRINT, stream)
+        free_after = torch.cuda.mem_get_info(gpu)[0]
         assert rc == lib.GEMM_OK, lib.status_string(rc)
+        if call == 1:
+            # Set up by the first call, the second allocates nothing: device
+            # memory is handed out in pages of at least 2 MiB, and a reload
+            # of the array would take 16 MiB.
+            assert free_before - free_after < (1 << 20), (free_before, free_after)
         rc, ref = _allocating(lib, scratch, FOOTPRINT, stream)
         assert rc == lib.GEMM_OK, lib.status_string(rc)
         assert got[0] > 0 and got[1] > 0

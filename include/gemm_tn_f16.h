@@ -214,6 +214,10 @@ int gemm_query_config(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt
 
 /* Synchronises `stream`, then returns and clears the device error word of the
  * current device: GEMM_OK, or GEMM_ERR_TIMEOUT if a kernel gave up waiting.
+ * The word is one per device, shared by every stream and every call of this
+ * library on the device: a timeout raised by a call on another stream is
+ * reported (and cleared) by whichever poll reads the word first, and a poll
+ * of `stream` does not wait for the other streams.
  * If `raw` is not NULL it receives the raw word (low byte = status, next byte
  * = the wait site that gave up: 1 producer/empty, 2 mma/full, 3 mma/tmem-empty,
  * 4 epilogue/tmem-full). */

@@ -609,7 +609,7 @@ def bench_config(tag, binding, torch, dev, stream, l2, peaks, peak_src, clocks):
              "roofline_ms": max(flops / (float(peaks["bf16_tflops"]) * 1e12),
                                 alg_bytes / (float(peaks["hbm_gbs"]) * 1e9)) * 1e3,
              "plan": {k: cfg[k] for k in ("path", "bn", "kstage", "katoms", "ctas", "epi_warps",
-                                          "b_resident", "wide")},
+                                          "b_resident", "wide", "small_m")},
              "l2": f"{R} operand copies ({R * int(alg_bytes) >> 20} MiB > 3 x L2) cycled",
              "clocks": clk}
     entry["roofline_frac"] = entry["roofline_ms"] / ms
@@ -676,7 +676,7 @@ def run_gpu(args, tag):
     opts = {"path": ["auto", "square", "skinny", "pair"].index(args.path), "bn": args.bn,
             "kstage": args.kstage, "katoms": args.katoms, "group_m": args.group_m,
             "epi_warps": args.epi_warps, "b_resident": args.b_resident, "pdl": args.pdl,
-            "wide": args.wide}
+            "wide": args.wide, "small_m": args.small_m}
     forced = any(opts.values())
     cfg = binding.query_config(M, N, K, b_layout=1 if spec.get("b_kn") else 0,
                                acc_f16=1 if spec.get("acc_f16") else 0, **opts)
@@ -935,6 +935,7 @@ def run_gpu(args, tag):
                                                             2 if cfg["wide"] else 1,
                                                             flag(scaled))
                       if cfg["path"] == 3 else
+                      "gemm_tn_f16_skinny<%s>" % flag(direct_d) if cfg["small_m"] else
                       "gemm_tn_f16_persistent<%d, %s, %s>" % (cfg["epi_warps"],
                                                               flag(cfg["b_resident"]),
                                                               flag(direct_d)))
@@ -966,7 +967,7 @@ def run_gpu(args, tag):
                 "bn": cfg["bn"], "bk": cfg["bk"], "kstage": cfg["kstage"], "ctas": cfg["ctas"],
                 "tiles": cfg["tiles"], "katoms": cfg["katoms"], "epi_warps": cfg["epi_warps"],
                 "b_resident": cfg["b_resident"], "pdl": cfg["pdl"], "wide": cfg["wide"],
-                "forced": forced}),
+                "small_m": cfg["small_m"], "forced": forced}),
             "launch_ms": ({"mean": ms, "median": statistics.median(launches_ms),
                            "p10": float(np.percentile(launches_ms, 10)),
                            "p90": float(np.percentile(launches_ms, 90))}
@@ -1051,6 +1052,9 @@ def main():
                     help="diagnostics: 1 = launch without programmatic dependent launch")
     ap.add_argument("--wide", type=int, default=0, choices=[0, 1, 2],
                     help="diagnostics: pair units of two n-tiles (0 choose, 1 never, 2 always)")
+    ap.add_argument("--small-m", type=int, default=0, choices=[0, 1, 2],
+                    help="diagnostics: the small-M kernel, one tile per CTA (0 choose, 1 never, "
+                         "2 always)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

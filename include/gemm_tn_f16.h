@@ -43,7 +43,8 @@ typedef enum {
 enum {
   GEMM_PATH_AUTO = 0,    /* choose from the shape */
   GEMM_PATH_SQUARE = 1,  /* persistent 128 x BN tiles, compute-bound shapes */
-  GEMM_PATH_SKINNY = 2,  /* M <= 128: one M tile, N spread over every SM, B streamed once */
+  GEMM_PATH_SKINNY = 2,  /* M <= 128: one M tile, N spread over every SM, B streamed once
+                            (the small-M kernel; see gemm_options_t.small_m) */
   GEMM_PATH_PAIR = 3     /* persistent 256 x BN tiles over CTA pairs (tcgen05 cta_group::2) */
 };
 
@@ -109,6 +110,14 @@ typedef struct {
                           ring carries A once per two B halves and both TMEM
                           accumulators hold the unit, so the same shared memory
                           holds a deeper ring.  Results are bit-identical. */
+  int small_m;         /* skinny path (M <= 128): 0 = choose, 1 = never, 2 = always (else
+                          GEMM_ERR_INVALID_VALUE).  The small-M kernel computes one
+                          128 x bn tile per CTA (so at most one n-tile per SM) and
+                          stages its epilogue in its ring once the tile's MMAs are
+                          done, so the whole shared memory holds the ring (four
+                          stages at bn = 96 where the single-CTA kernel fits three).
+                          Otherwise the single-CTA kernel runs.  With the same
+                          katoms the results are bit-identical. */
 } gemm_options_t;
 
 /* gemm_tn_f16 with an explicit configuration (sweeps, tests).  Same
@@ -208,6 +217,7 @@ typedef struct {
   int pdl;             /* 1: launched with programmatic stream serialization */
   int wide;            /* 1: pair units of two adjacent n-tiles (tiles still counts
                           output tiles; the grid is sized by units) */
+  int small_m;         /* 1: the small-M kernel (one tile per CTA) */
 } gemm_config_t;
 int gemm_query_config(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt,
                       gemm_config_t* out);

@@ -353,7 +353,9 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
         acc_phase ^= 1u;
       }
     }
-    if (lane == 0) bulk_wait_group_all();
+    // The staging buffers must have been read before the CTA's shared memory
+    // is released; the stores themselves complete with the grid.
+    if (lane == 0) bulk_wait_group_read<0>();
     __syncwarp();
   }
 

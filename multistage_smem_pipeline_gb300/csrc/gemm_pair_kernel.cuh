@@ -63,7 +63,12 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
   uint8_t* const smem = smem_raw + (base - raw);
   constexpr int kThreads = threads_for(kEpiWarps);
   constexpr int kChunkStride = kEpiWarps / 4;  // warps sharing a TMEM lane quadrant
-  constexpr int kEpiBatch = 4;                  // TMEM chunks read per wait in the epilogue
+  // TMEM chunks read per wait in the epilogue.  The plain epilogue rounds a
+  // batch to fp16 as soon as it is in registers (64 registers live for four
+  // chunks); the scaled one keeps fp32 until C is applied, and the direct
+  // stores need registers of their own, so those read two chunks at a time
+  // to stay within the 168 registers of an 8-warp CTA.
+  constexpr int kEpiBatch = (kScaled || kDirectD) ? 2 : 4;
   const SmemLayout L = SmemLayout::make(p.stages, p.stage_bytes, kEpiWarps);
 
   const int warp = threadIdx.x >> 5;
@@ -280,11 +285,23 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(leader_tempty);
           }
+          if (!kScaled) {
+            // Round the batch to fp16 now, in place: r[b][i] holds columns 2i
+            // and 2i + 1.  An fp16 accumulator's bits are taken as they are
+            // (the low 16 bits of each TMEM column), which is exactly what
+            // widening to fp32 and rounding back gives.
+#pragma unroll
+            for (int b = 0; b < kEpiBatch; ++b)
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                r[b][i] = p.acc_f16 ? ((r[b][2 * i] & 0xffffu) | (r[b][2 * i + 1] << 16))
+                                    : pack_half2(r[b][2 * i], r[b][2 * i + 1]);
+          }
 #pragma unroll
           for (int b = 0; b < kEpiBatch; ++b) {
             const int c = c0 + b * kChunkStride;
             if (c > last_c) break;
-            if (p.acc_f16) widen_f16_accumulator(r[b]);
+            if (kScaled && p.acc_f16) widen_f16_accumulator(r[b]);
             const uint32_t buf = my_bufs + (chunk_seq % kEpiBufs) * kEpiChunkBytes;
             const bool with_c = kScaled && p.beta != 0.0f;
             if (!(with_c && c_ahead) && chunk_seq >= static_cast<uint32_t>(kEpiBufs)) {
@@ -321,10 +338,15 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
             const uint32_t sw = (lane >> 1) & 3u;
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
-              st_shared_v4(row_addr + ((v ^ sw) << 4), pack_half2(r[b][8 * v + 0], r[b][8 * v + 1]),
-                           pack_half2(r[b][8 * v + 2], r[b][8 * v + 3]),
-                           pack_half2(r[b][8 * v + 4], r[b][8 * v + 5]),
-                           pack_half2(r[b][8 * v + 6], r[b][8 * v + 7]));
+              if (kScaled)
+                st_shared_v4(row_addr + ((v ^ sw) << 4),
+                             pack_half2(r[b][8 * v + 0], r[b][8 * v + 1]),
+                             pack_half2(r[b][8 * v + 2], r[b][8 * v + 3]),
+                             pack_half2(r[b][8 * v + 4], r[b][8 * v + 5]),
+                             pack_half2(r[b][8 * v + 6], r[b][8 * v + 7]));
+              else
+                st_shared_v4(row_addr + ((v ^ sw) << 4), r[b][4 * v], r[b][4 * v + 1],
+                             r[b][4 * v + 2], r[b][4 * v + 3]);
             }
             if (kDirectD) {
               __syncwarp();
@@ -352,7 +374,9 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
         acc_phase ^= 1u;
       }
     }
-    if (lane == 0) bulk_wait_group_all();
+    // The staging buffers must have been read before the CTA's shared memory
+    // is released; the stores themselves complete with the grid.
+    if (lane == 0) bulk_wait_group_read<0>();
     __syncwarp();
   }
 

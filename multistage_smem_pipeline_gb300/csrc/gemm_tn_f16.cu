@@ -12,6 +12,7 @@
 #include <mutex>
 
 #include "gemm_pair_kernel.cuh"
+#include "gemm_skinny_kernel.cuh"
 #include "gemm_tn_f16.h"
 #include "host.cuh"
 
@@ -33,6 +34,7 @@ constexpr int kMaxDynSmem = 232448;  // 227 KiB opt-in limit per CTA on sm_100-c
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 constexpr int kMaxResidentN = 4;  // n-blocks a resident-B plan may have
 constexpr int64_t kWideMinK = 4096;  // shortest k loop for which wide pair units are chosen
+constexpr int kSkinnyKatoms = 2;     // K slices per stage of the small-M kernel's ring
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -121,7 +123,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
       o.kstage == 1 || o.kstage > kMaxStages || o.max_ctas < 0 || o.group_m < 0 || o.inject < 0 ||
       o.inject > 1 || o.katoms < 0 || o.katoms > 2 || o.acc_f16 < 0 || o.acc_f16 > 1 ||
       o.b_resident < 0 || o.b_resident > 2 || o.pdl < 0 || o.pdl > 1 || o.wide < 0 ||
-      o.wide > 2 ||
+      o.wide > 2 || o.small_m < 0 || o.small_m > 2 ||
       (o.epi_warps != 0 && o.epi_warps != 4 && o.epi_warps != 8))
     return GEMM_ERR_INVALID_VALUE;
   if (o.path == GEMM_PATH_SKINNY && M > kBM) return GEMM_ERR_INVALID_VALUE;
@@ -246,13 +248,41 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
     }
     if (o.b_resident == 2 && !b_resident) return GEMM_ERR_INVALID_VALUE;
   }
+  // The small-M kernel on the skinny path: one tile per CTA (so at most one
+  // n-tile per SM), its epilogue staged in the ring once the tile's MMAs are
+  // done, so the whole shared memory holds the ring.  It has four epilogue
+  // warps.
+  int64_t ctas_cap = sms;
+  if (o.max_ctas) ctas_cap = std::min<int64_t>(ctas_cap, o.max_ctas);
+  const bool small_possible = path == GEMM_PATH_SKINNY && !b_resident && num_n <= ctas_cap &&
+                              (o.epi_warps == 0 || o.epi_warps == kSkinnyEpiWarps);
+  if (o.small_m == 2 && !small_possible) return GEMM_ERR_INVALID_VALUE;
+  const bool small_m = small_possible && o.small_m != 1;
+  if (small_m) {
+    epi_warps = kSkinnyEpiWarps;
+    katoms = o.katoms ? o.katoms : kSkinnyKatoms;
+  }
   const int64_t num_k = (K + kBK * katoms - 1) / (kBK * katoms);
-  const uint32_t stage_bytes = b_resident ? static_cast<uint32_t>(katoms) * kABytes
-                                          : stage_bytes_for(path, bn, katoms, nt);
-  const int fit = stages_that_fit(stage_bytes, epi_warps, bres_bytes);
-  if (fit < 2) return GEMM_ERR_INVALID_VALUE;
-  const int stages = o.kstage ? o.kstage : fit;
-  if (stages > fit) return GEMM_ERR_INVALID_VALUE;
+  uint32_t stage_bytes = b_resident ? static_cast<uint32_t>(katoms) * kABytes
+                                    : stage_bytes_for(path, bn, katoms, nt);
+  int stages = 0;
+  uint32_t smem_total = 0;
+  if (small_m) {
+    const auto small_total = [&](int sc) { return SkinnyLayout::make(sc, stage_bytes).total + 1024; };
+    int fit = 1;
+    while (fit + 1 <= kMaxStages && small_total(fit + 1) <= static_cast<uint32_t>(kMaxDynSmem))
+      ++fit;
+    if (fit < 2) return GEMM_ERR_INVALID_VALUE;
+    stages = o.kstage ? o.kstage : fit;
+    if (stages > fit) return GEMM_ERR_INVALID_VALUE;
+    smem_total = small_total(stages);
+  } else {
+    const int fit = stages_that_fit(stage_bytes, epi_warps, bres_bytes);
+    if (fit < 2) return GEMM_ERR_INVALID_VALUE;
+    stages = o.kstage ? o.kstage : fit;
+    if (stages > fit) return GEMM_ERR_INVALID_VALUE;
+    smem_total = SmemLayout::make(stages, stage_bytes, epi_warps, bres_bytes).total + 1024;
+  }
   // Balanced grids: as many CTAs (pairs) as the fewest waves need, so every
   // one gets the same number of tiles (units) to one.  An HBM-bound stream
   // then has no partial last wave (tall 81920 x 256 x 256: 640 tiles as 5 on
@@ -266,7 +296,9 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
     return std::min<int64_t>(slots, (even + multiple - 1) / multiple * multiple);
   };
   int ctas;
-  if (path == GEMM_PATH_PAIR) {
+  if (small_m) {
+    ctas = static_cast<int>(tiles);  // one tile each
+  } else if (path == GEMM_PATH_PAIR) {
     int64_t pairs = std::min<int64_t>(units, max_pairs);
     if (o.max_ctas) pairs = std::min<int64_t>(pairs, std::max(1, o.max_ctas / 2));
     ctas = static_cast<int>(2 * balanced(units, pairs, 1));
@@ -278,7 +310,6 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   const int group_m =
       o.group_m ? o.group_m
                 : (path == GEMM_PATH_PAIR ? (wide ? 16 : 8) : (b_resident && num_n > 1 ? 1 : 16));
-  const SmemLayout L = SmemLayout::make(stages, stage_bytes, epi_warps, bres_bytes);
 
   Plan pl;
   std::memset(&pl, 0, sizeof(pl));
@@ -292,11 +323,13 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   pl.cfg.ctas = ctas;
   pl.cfg.group_m = group_m;
   pl.cfg.tiles = static_cast<int>(tiles);
-  pl.cfg.smem_bytes = static_cast<int>(L.total + 1024);  // + alignment slack
-  pl.cfg.tmem_cols = static_cast<int>(pow2_at_least(2u * bn));
+  pl.cfg.smem_bytes = static_cast<int>(smem_total);  // includes 1 KiB of alignment slack
+  // two accumulators (consecutive tiles overlap), one in the small-M kernel
+  pl.cfg.tmem_cols = static_cast<int>(pow2_at_least(small_m ? bn : 2u * bn));
   pl.cfg.b_resident = b_resident ? 1 : 0;
   pl.cfg.pdl = o.pdl ? 0 : 1;
   pl.cfg.wide = wide ? 1 : 0;
+  pl.cfg.small_m = small_m ? 1 : 0;
 
   GemmParams& p = pl.p;
   p.M = static_cast<int32_t>(M);
@@ -314,7 +347,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   if (o.acc_f16) p.idesc &= ~(3u << 4);                      // bits 4-5: D format F16
   p.acc_f16 = o.acc_f16;
   p.b_kn = b_kn;
-  p.tmem_cols = pow2_at_least(2u * bn);
+  p.tmem_cols = static_cast<uint32_t>(pl.cfg.tmem_cols);
   p.stage_bytes = stage_bytes;
   p.b_atom_bytes = b_atom_bytes_for(path, bn);
   p.katoms = katoms;
@@ -355,7 +388,8 @@ bool grant_smem(Kernel k) {
 // x scaled epilogue for the pair.
 template <bool kDirectD>
 bool grant_all(bool ok) {
-  return ok && grant_smem(gemm_tn_f16_persistent<4, false, kDirectD>) &&
+  return ok && grant_smem(gemm_tn_f16_skinny<kDirectD>) &&
+         grant_smem(gemm_tn_f16_persistent<4, false, kDirectD>) &&
          grant_smem(gemm_tn_f16_persistent<8, false, kDirectD>) &&
          grant_smem(gemm_tn_f16_persistent<4, true, kDirectD>) &&
          grant_smem(gemm_tn_f16_persistent<8, true, kDirectD>) &&
@@ -386,8 +420,9 @@ cudaError_t launch_pair(const cudaLaunchConfig_t& cfg, int epi_warps, const CUte
 
 template <bool kDirectD>
 cudaError_t launch_kernel(const cudaLaunchConfig_t& cfg, bool pair, bool wide, bool resident,
-                          int epi_warps, const CUtensorMap& a, const CUtensorMap& b,
+                          bool small, int epi_warps, const CUtensorMap& a, const CUtensorMap& b,
                           const CUtensorMap& d, const GemmParams& p) {
+  if (small) return cudaLaunchKernelEx(&cfg, gemm_tn_f16_skinny<kDirectD>, a, b, d, p);
   if (pair)
     return wide ? launch_pair<kDirectD, 2>(cfg, epi_warps, a, b, d, p)
                 : launch_pair<kDirectD, 1>(cfg, epi_warps, a, b, d, p);
@@ -574,16 +609,17 @@ int launch_gemm(int64_t M, int64_t N, int64_t K, const View& a, const View& b, c
     ++nattr;
   }
   cfg.gridDim = dim3(pl.cfg.ctas, 1, 1);
-  cfg.blockDim = dim3(threads_for(pl.cfg.epi_warps), 1, 1);
+  cfg.blockDim = dim3(pl.cfg.small_m ? kSkinnyThreads : threads_for(pl.cfg.epi_warps), 1, 1);
   cfg.dynamicSmemBytes = pl.cfg.smem_bytes;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = nattr;
-  const bool wide = pl.cfg.wide != 0, res = pl.p.b_resident != 0;
+  const bool wide = pl.cfg.wide != 0, res = pl.p.b_resident != 0, small = pl.cfg.small_m != 0;
   const cudaError_t e =
-      d_direct
-          ? launch_kernel<true>(cfg, pair, wide, res, pl.cfg.epi_warps, tmA, tmB, tmD, pl.p)
-          : launch_kernel<false>(cfg, pair, wide, res, pl.cfg.epi_warps, tmA, tmB, tmD, pl.p);
+      d_direct ? launch_kernel<true>(cfg, pair, wide, res, small, pl.cfg.epi_warps, tmA, tmB, tmD,
+                                     pl.p)
+               : launch_kernel<false>(cfg, pair, wide, res, small, pl.cfg.epi_warps, tmA, tmB,
+                                      tmD, pl.p);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return GEMM_ERR_LAUNCH;

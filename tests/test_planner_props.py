@@ -32,7 +32,9 @@ def _check(cfg, M, N, K):
     assert cfg["katoms"] in (1, 2) and cfg["bk"] == 64 * cfg["katoms"]
     assert cfg["epi_warps"] in (4, 8)
     assert 32 <= cfg["bn"] <= 256 and cfg["bn"] % 32 == 0
-    assert cfg["tmem_cols"] >= 2 * cfg["bn"] and cfg["tmem_cols"] <= TMEM_COLS
+    # two accumulators, or one in the small-M kernel (one tile per CTA)
+    accs = 1 if cfg["small_m"] else 2
+    assert cfg["tmem_cols"] >= accs * cfg["bn"] and cfg["tmem_cols"] <= TMEM_COLS
     assert cfg["tmem_cols"] & (cfg["tmem_cols"] - 1) == 0          # a power of two
     bm = 256 if cfg["path"] == 3 else 128
     assert cfg["bm"] == bm
@@ -42,6 +44,9 @@ def _check(cfg, M, N, K):
         assert cfg["ctas"] % 2 == 0                                    # whole clusters of 2
     if cfg["path"] == 2:
         assert M <= 128
+    if cfg["small_m"]:
+        assert cfg["path"] == 2 and cfg["ctas"] == cfg["tiles"] and cfg["epi_warps"] == 4
+        assert not cfg["b_resident"] and not cfg["wide"]
     if cfg["wide"]:
         units = -(-M // 256) * -(-(-(-N // cfg["bn"])) // 2)
         assert cfg["path"] == 3 and cfg["ctas"] <= 2 * units and not cfg["b_resident"]
@@ -71,7 +76,8 @@ def test_default_plans_fit(binding):
                                   dict(epi_warps=4), dict(epi_warps=8), dict(b_resident=1),
                                   dict(acc_f16=1), dict(b_layout=1), dict(max_ctas=37),
                                   dict(wide=2), dict(wide=2, path=3, epi_warps=8),
-                                  dict(wide=1)])
+                                  dict(wide=1), dict(small_m=1), dict(small_m=2),
+                                  dict(small_m=2, katoms=1)])
 def test_forced_plans_fit_or_are_refused(binding, opts):
     accepted = 0
     for M, N, K in _shapes(600, 502 + len(str(opts))):
@@ -94,6 +100,8 @@ def test_forced_plans_fit_or_are_refused(binding, opts):
             assert cfg["wide"] == 1
         if opts.get("wide") == 1:
             assert cfg["wide"] == 0
+        if "small_m" in opts:
+            assert cfg["small_m"] == (1 if opts["small_m"] == 2 else 0)
         if opts.get("b_resident") == 1:
             assert cfg["b_resident"] == 0
         if opts.get("b_layout") == 1:

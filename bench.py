@@ -75,7 +75,7 @@ def load_peaks():
 # The sources that decide the GEMM kernel's code and its launch plan: the
 # recorded DRAM traffic stays valid while these are unchanged.
 KERNEL_SOURCES = ("ptx.cuh", "pipeline.cuh", "gemm_kernel.cuh", "gemm_pair_kernel.cuh",
-                  "gemm_tn_f16.cu")
+                  "gemm_skinny_kernel.cuh", "gemm_tn_f16.cu")
 
 
 def code_tokens(text: str) -> str:

@@ -118,6 +118,15 @@ typedef struct {
                           stages at bn = 96 where the single-CTA kernel fits three).
                           Otherwise the single-CTA kernel runs.  With the same
                           katoms the results are bit-identical. */
+  int split_k;         /* 0 = choose, 1 = never, 2 = always (else GEMM_ERR_INVALID_VALUE).
+                          Split: a cluster of two CTAs computes each 128 x bn tile,
+                          each CTA half of the k range; the two exchange their fp32
+                          partials through distributed shared memory and each
+                          rounds and stores half of the tile.  For short k loops
+                          whose tiles fit in one wave of CTA pairs (1024^3).  Needs
+                          an N x K B, an fp32 accumulator and aligned D rows;
+                          results differ from the unsplit sum only in fp32
+                          rounding (bit-exact where the partial sums are). */
 } gemm_options_t;
 
 /* gemm_tn_f16 with an explicit configuration (sweeps, tests).  Same
@@ -218,6 +227,7 @@ typedef struct {
   int wide;            /* 1: pair units of two adjacent n-tiles (tiles still counts
                           output tiles; the grid is sized by units) */
   int small_m;         /* 1: the small-M kernel (one tile per CTA) */
+  int split_k;         /* 1: k split over a CTA pair (ctas = 2 x tiles) */
 } gemm_config_t;
 int gemm_query_config(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt,
                       gemm_config_t* out);

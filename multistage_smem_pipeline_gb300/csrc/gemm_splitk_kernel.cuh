@@ -1,0 +1,307 @@
+// Split-K fp16 TN GEMM over a CTA pair, for shapes whose k loops are short
+// enough that each CTA's fill and MMA issue set the time (1024^3: one wave of
+// 128 x 64 tiles, each CTA pulling 384 KiB through its SM for 8 k-blocks).
+//
+// A cluster of two CTAs owns one 128 x BN tile of D.  CTA r multiplies the
+// r-th half of the k range into its own TMEM accumulator (the pipeline of
+// "cute(9) multistage_gemm": a ring of K-tiles filled ahead of the MMAs,
+// guarded by full and empty barriers, here TMA loads and tcgen05.mma).  Then
+// each CTA finalises half of the tile's columns: CTA r keeps columns
+// [r BN/2, (r+1) BN/2), sends its fp32 partial of the other half into the
+// peer's shared memory (st.shared::cluster), receives the peer's partial of
+// its own half, adds the two, rounds to fp16 and stores D.  Per CTA that is
+// half the k-blocks of a 128 x BN tile -- at 1024^3 with BN = 128, 256 KiB of
+// operands and 32 MMAs per CTA instead of 384 KiB and 64 for a 128 x 64 tile
+// over the whole k range -- for a 32 KiB exchange.
+//
+// The exchange reuses the ring: once a CTA's MMAs have completed, nothing
+// fills or reads its ring any more (one tile per cluster), so the epilogue's
+// staging buffers take its first 16 KiB and the peer's partial the next
+// 128 x BN/2 x 4 bytes.  Two barriers per CTA order it, each completed by
+// the 128 epilogue threads of the peer with release at cluster scope and
+// waited on with acquire at cluster scope:
+//   peer_free  -- "my MMAs are done, you may write into my ring";
+//   rx_full    -- "my partial of your half is in your ring".
+// The final value of an element is p0 + p1 in fp32 whichever CTA forms it,
+// so the result does not depend on the pair's timing.  Every wait is
+// bounded; both CTAs meet on a cluster barrier before either exits.
+#pragma once
+#include "gemm_kernel.cuh"
+
+namespace gb300 {
+
+constexpr int kSplitEpiWarps = 4;
+constexpr int kSplitThreads = 64 + 32 * kSplitEpiWarps;  // producer, MMA, epilogue
+constexpr int kSplitPeerArrivals = 32 * kSplitEpiWarps;   // the peer's epilogue threads
+constexpr uint32_t kSplitStagingBytes = kSplitEpiWarps * kEpiBufs * kEpiChunkBytes;  // 16 KiB
+
+// Bytes the ring must hold for the exchange: the staging buffers, then the
+// peer's fp32 partial of this CTA's BN/2 columns.
+__host__ __device__ constexpr uint32_t splitk_exchange_bytes(int bn) {
+  return kSplitStagingBytes + static_cast<uint32_t>(bn) * 256u;
+}
+
+// Shared-memory carve-up, offsets from the 1024-aligned base: the ring, then
+// the mbarriers full[S], empty[S], tmem-full, drain, peer-free, rx-full.
+struct SplitLayout {
+  uint32_t ring, bars, misc, total;
+  __host__ __device__ static SplitLayout make(int stages, uint32_t stage_bytes) {
+    SplitLayout L;
+    L.ring = 0;
+    L.bars = stages * stage_bytes;
+    L.misc = L.bars + 8 * (2 * stages + 4);
+    L.total = L.misc + 16;
+    return L;
+  }
+};
+
+// wait_or_abort with acquire at cluster scope (for barriers the peer arrives on).
+__device__ __forceinline__ bool wait_cluster_or_abort(uint32_t bar, uint32_t parity,
+                                                      uint64_t timeout_ns, volatile int* abort_flag,
+                                                      uint32_t site) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((it & 31u) == 0) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > timeout_ns) {
+        *abort_flag = 1;
+        record_error(kErrTimeout, site);
+        return false;
+      }
+    }
+  }
+}
+
+// The peer's partial of this CTA's half, 128 rows x BN/2 fp32 columns, as
+// 16-byte groups: group g (columns 4g..4g+3 of the half) of row `row` at
+// (g * 128 + row) * 16, so a warp's 32 rows of one group are 512 contiguous
+// bytes for both the peer's stores and this CTA's loads.
+__device__ __forceinline__ uint32_t splitk_rx_offset(int g, int row) {
+  return static_cast<uint32_t>(g * 128 + row) * 16u;
+}
+
+__global__ void __launch_bounds__(kSplitThreads, 1)
+    gemm_tn_f16_splitk(const __grid_constant__ CUtensorMap tmA,
+                       const __grid_constant__ CUtensorMap tmB,
+                       const __grid_constant__ CUtensorMap tmD, const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const smem = smem_raw + (base - raw);
+  const int S = p.stages;
+  const SplitLayout L = SplitLayout::make(S, p.stage_bytes);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const uint32_t peer = rank ^ 1u;
+  int mb, nb;
+  tile_coords(static_cast<int>(blockIdx.x >> 1), p, mb, nb);
+  // this CTA's k-blocks: the first ceil(nk/2) for rank 0, the rest for rank 1
+  const int h0 = (p.num_k_blocks + 1) / 2;
+  const int kb_lo = rank ? h0 : 0;
+  const int nkb = rank ? p.num_k_blocks - h0 : h0;
+  const uint32_t bars = base + L.bars;
+  auto full_bar = [&](int s) { return bars + 8u * s; };
+  auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
+  const uint32_t tfull_bar = bars + 8u * (2 * S);
+  const uint32_t drain_bar = bars + 8u * (2 * S + 1);
+  const uint32_t peer_free_bar = bars + 8u * (2 * S + 2);
+  const uint32_t rx_full_bar = bars + 8u * (2 * S + 3);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc + 4);
+
+  if (threadIdx.x == 0) {
+    grid_launch_dependents();  // see gemm_tn_f16_persistent
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    mbar_init(tfull_bar, 1);
+    mbar_init(drain_bar, 1);
+    mbar_init(peer_free_bar, kSplitPeerArrivals);
+    mbar_init(rx_full_bar, kSplitPeerArrivals);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmD);
+  }
+  __syncwarp();
+  cluster_sync();  // both CTAs' barriers exist before any remote arrive
+  uint32_t tmem_base = 0;
+  if (warp != 0) {
+    if (warp == 1) {
+      tmem_alloc(smem_u32(tmem_slot), p.tmem_cols);
+      tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    named_barrier_sync(1, kSplitThreads - 32);
+    tc_fence_after_sync();
+    tmem_base = *tmem_slot;
+  }
+  grid_dependency_wait();  // first global-memory access follows
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0;
+      for (int i = 0; i < nkb && !*abort_flag; ++i) {
+        const int kb = kb_lo + i;
+        if (!wait_or_abort(empty_bar(stage), phase ^ 1u, p.timeout_ns, abort_flag, kSiteEmpty))
+          break;
+        const uint32_t a_dst = base + L.ring + stage * p.stage_bytes;
+        const uint32_t b_dst = a_dst + p.katoms * kABytes;
+        mbar_arrive_expect_tx(full_bar(stage), p.stage_bytes);
+        if (!(p.inject == 1 && issued == 0)) {
+          for (int at = 0; at < p.katoms; ++at) {
+            const int x = (kb * p.katoms + at) * kBK;  // past K: the box reads zeros
+            tma_load_2d(a_dst + at * kABytes, &tmA, full_bar(stage), x, mb * kBM);
+            tma_load_2d(b_dst + at * p.b_atom_bytes, &tmB, full_bar(stage), x, nb * p.bn);
+          }
+        }
+        ++issued;
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      const uint32_t first = issued > static_cast<uint32_t>(S) ? issued - S : 0u;
+      for (uint32_t i = first; i < issued; ++i)
+        wait_timed(full_bar(i % S), (i / S) & 1u, p.timeout_ns);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int i = 0; i < nkb; ++i) {
+        if (!wait_or_abort(full_bar(stage), phase, p.timeout_ns, abort_flag, kSiteFull)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t a_src = base + L.ring + stage * p.stage_bytes;
+        const uint32_t b_src = a_src + p.katoms * kABytes;
+        for (int at = 0; at < p.katoms; ++at) {
+          const uint64_t a_desc = sw128_kmajor_desc(a_src + at * kABytes);
+          const uint64_t b_desc = sw128_kmajor_desc(b_src + at * p.b_atom_bytes);
+#pragma unroll
+          for (int k = 0; k < kBK / kUmmaK; ++k)
+            umma_f16(tmem_base, a_desc + 2u * k, b_desc + 2u * k, p.idesc, (i | at | k) != 0);
+        }
+        umma_commit(empty_bar(stage));
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (ok) umma_commit(tfull_bar);
+      umma_commit(drain_bar);
+      wait_timed(drain_bar, 0, p.timeout_ns);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2..5)
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int row = q * 32 + lane;
+    const int m0 = mb * kBM + q * 32;
+    const bool rows_live = m0 < p.M;
+    const int half = p.bn / 2;  // a multiple of 32
+    const uint32_t ring = base + L.ring;
+    const uint32_t my_bufs = ring + (warp - 2) * kEpiBufs * kEpiChunkBytes;
+    const uint32_t rx = ring + kSplitStagingBytes;
+    const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    int ok = 0;
+    if (lane == 0) ok = wait_or_abort(tfull_bar, 0, p.timeout_ns, abort_flag, kSiteTmemFull);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) {
+      tc_fence_after_sync();
+      fence_proxy_async_smem();  // the ring's last async-proxy uses precede the writes below
+      // 1. this CTA's MMAs are done: the peer may write into its ring
+      mbar_arrive_cluster(mapa_shared(peer_free_bar, peer));
+      // 2. once the peer's are done too, send it this CTA's partial of its half
+      // (every thread acquires the peer's arrivals; the warp goes on only if
+      // all did, so the tcgen05.ld below stays warp-uniform)
+      if (__all_sync(0xffffffffu, wait_cluster_or_abort(peer_free_bar, 0, p.timeout_ns,
+                                                        abort_flag, kSiteTmemFull))) {
+        if (rows_live) {
+          const uint32_t peer_rx = mapa_shared(rx, peer);
+          for (int c = 0; c < half / kEpiCols; ++c) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(peer * half + c * kEpiCols), r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int g = 0; g < 8; ++g)
+              st_cluster_v4(peer_rx + splitk_rx_offset(c * 8 + g, row), r[4 * g], r[4 * g + 1],
+                            r[4 * g + 2], r[4 * g + 3]);
+          }
+        }
+        // release: this thread's stores above are visible to the peer's acquire
+        mbar_arrive_cluster(mapa_shared(rx_full_bar, peer));
+        // 3. the peer's partial of this CTA's half: add, round, store
+        if (__all_sync(0xffffffffu, wait_cluster_or_abort(rx_full_bar, 0, p.timeout_ns,
+                                                          abort_flag, kSiteTmemFull)) &&
+            rows_live) {
+          const int n0 = nb * p.bn + static_cast<int>(rank) * half;
+          const int nchunks = (min(half, p.N - n0) + kEpiCols - 1) / kEpiCols;
+          for (int c = 0; c < nchunks; ++c) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(rank * half + c * kEpiCols), r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+              const uint4 v = ld_shared_v4(rx + splitk_rx_offset(c * 8 + g, row));
+              r[4 * g] = __float_as_uint(__uint_as_float(r[4 * g]) + __uint_as_float(v.x));
+              r[4 * g + 1] = __float_as_uint(__uint_as_float(r[4 * g + 1]) + __uint_as_float(v.y));
+              r[4 * g + 2] = __float_as_uint(__uint_as_float(r[4 * g + 2]) + __uint_as_float(v.z));
+              r[4 * g + 3] = __float_as_uint(__uint_as_float(r[4 * g + 3]) + __uint_as_float(v.w));
+            }
+            const uint32_t buf = my_bufs + (c % kEpiBufs) * kEpiChunkBytes;
+            if (c >= kEpiBufs) {
+              if (lane == 0) bulk_wait_group_read<kEpiBufs - 1>();
+              __syncwarp();
+            }
+            if (p.scaled) {
+              const bool with_c = p.beta != 0.0f;
+              if (with_c) stage_c_chunk(p, m0, n0 + c * kEpiCols, lane, buf);
+              apply_alpha_beta(r, p, with_c, buf, lane);
+            }
+            const uint32_t row_addr = buf + lane * 64u;
+            const uint32_t sw = (lane >> 1) & 3u;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              st_shared_v4(row_addr + ((j ^ sw) << 4), pack_half2(r[8 * j + 0], r[8 * j + 1]),
+                           pack_half2(r[8 * j + 2], r[8 * j + 3]),
+                           pack_half2(r[8 * j + 4], r[8 * j + 5]),
+                           pack_half2(r[8 * j + 6], r[8 * j + 7]));
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmD, buf, n0 + c * kEpiCols, m0);
+              bulk_commit_group();
+            }
+          }
+        }
+      }
+    }
+    if (lane == 0) bulk_wait_group_read<0>();
+    __syncwarp();
+  }
+
+  __syncwarp();
+  tc_fence_before_sync();
+  cluster_sync();  // no remote store or arrive targets a CTA that has left
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, p.tmem_cols);
+  }
+}
+
+}  // namespace gb300

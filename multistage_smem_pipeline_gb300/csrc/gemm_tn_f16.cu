@@ -13,6 +13,7 @@
 
 #include "gemm_pair_kernel.cuh"
 #include "gemm_skinny_kernel.cuh"
+#include "gemm_splitk_kernel.cuh"
 #include "gemm_tn_f16.h"
 #include "host.cuh"
 
@@ -115,7 +116,7 @@ struct Plan {
 };
 
 int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sms, int max_pairs,
-              Plan* out, int b_kn = 0) {
+              Plan* out, int b_kn = 0, bool direct_d = false) {
   gemm_options_t o;
   std::memset(&o, 0, sizeof(o));
   if (opt) o = *opt;
@@ -123,7 +124,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
       o.kstage == 1 || o.kstage > kMaxStages || o.max_ctas < 0 || o.group_m < 0 || o.inject < 0 ||
       o.inject > 1 || o.katoms < 0 || o.katoms > 2 || o.acc_f16 < 0 || o.acc_f16 > 1 ||
       o.b_resident < 0 || o.b_resident > 2 || o.pdl < 0 || o.pdl > 1 || o.wide < 0 ||
-      o.wide > 2 || o.small_m < 0 || o.small_m > 2 ||
+      o.wide > 2 || o.small_m < 0 || o.small_m > 2 || o.split_k < 0 || o.split_k > 2 ||
       (o.epi_warps != 0 && o.epi_warps != 4 && o.epi_warps != 8))
     return GEMM_ERR_INVALID_VALUE;
   if (o.path == GEMM_PATH_SKINNY && M > kBM) return GEMM_ERR_INVALID_VALUE;
@@ -190,6 +191,63 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   if (bn == 0) return GEMM_ERR_INVALID_VALUE;
   if (path == GEMM_PATH_SQUARE && M <= kBM && o.path != GEMM_PATH_SQUARE) path = GEMM_PATH_SKINNY;
 
+  // Split K over a CTA pair: for short k loops whose 128 x bn tiles fit in
+  // one wave of pairs, each CTA of a pair takes half the k-blocks and the two
+  // exchange fp32 partials through distributed shared memory.  bn is the
+  // narrowest multiple of 64 (each CTA keeps half the columns, whole 32-column
+  // chunks) whose tiles fit the co-resident pairs; the ring must also hold the
+  // exchange once the MMAs are done.  Chosen by itself for single-CTA plans of
+  // one wave with 512 <= K <= 1024 (measured: 1024^3).
+  const int64_t tiles_1 = ((M + kBM - 1) / kBM) * ((N + bn - 1) / bn);  // the unsplit plan's
+  int split_bn = 0, split_katoms = 0, split_stages = 0;
+  uint32_t split_stage_bytes = 0;
+  {
+    const bool kind_ok = !b_kn && !o.acc_f16 && !direct_d && o.b_resident != 2 && o.wide != 2 &&
+                         o.small_m != 2 && (o.path == GEMM_PATH_AUTO || o.path == GEMM_PATH_SQUARE) &&
+                         (o.epi_warps == 0 || o.epi_warps == kSplitEpiWarps);
+    int64_t pair_cap = max_pairs;
+    if (o.max_ctas) pair_cap = std::min<int64_t>(pair_cap, o.max_ctas / 2);
+    for (int cand = 64; kind_ok && cand <= 256 && !split_bn; cand += 64) {
+      if (o.bn && cand != o.bn) continue;
+      const int64_t t = ((M + kBM - 1) / kBM) * ((N + cand - 1) / cand);
+      if (t > pair_cap) continue;
+      // K slices per stage: 2 when the ring still gets 3 stages, as elsewhere
+      int ka = 0, fit = 0;
+      uint32_t sb = 0;
+      for (int k2 : {2, 1}) {
+        if (ka || (o.katoms && k2 != o.katoms)) continue;
+        const uint32_t b = static_cast<uint32_t>(k2) * (kABytes + static_cast<uint32_t>(cand) * 128u);
+        int f = 1;
+        while (f + 1 <= kMaxStages &&
+               SplitLayout::make(f + 1, b).total + 1024 <= static_cast<uint32_t>(kMaxDynSmem))
+          ++f;
+        if (k2 == 2 && !o.katoms && f < 3) continue;
+        ka = k2;
+        fit = f;
+        sb = b;
+      }
+      // this is the tile width; the plan stands or falls with it
+      const int st = o.kstage ? o.kstage : fit;
+      if (!ka || (K + kBK * ka - 1) / (kBK * ka) < 2 ||  // a k-block for each CTA at least
+          st < 2 || st > fit || st * sb < splitk_exchange_bytes(cand))
+        break;
+      split_bn = cand;
+      split_katoms = ka;
+      split_stages = st;
+      split_stage_bytes = sb;
+    }
+  }
+  if (o.split_k == 2 && !split_bn) return GEMM_ERR_INVALID_VALUE;
+  const bool split_k =
+      split_bn && (o.split_k == 2 ||
+                   (o.split_k == 0 && path == GEMM_PATH_SQUARE && o.b_resident == 0 && M > kBM &&
+                    K >= 512 && K <= 1024 && tiles_1 <= sms));
+  if (split_k) {
+    bn = split_bn;
+    path = GEMM_PATH_SQUARE;
+    nt = 1;
+  }
+
   const int bm = (path == GEMM_PATH_PAIR) ? 2 * kBM : kBM;
   const int64_t num_m = (M + bm - 1) / bm;
   const int64_t num_n = (N + bn - 1) / bn;
@@ -225,7 +283,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   int64_t ctas_1 = std::min<int64_t>(tiles, sms);
   if (o.max_ctas) ctas_1 = std::min<int64_t>(ctas_1, o.max_ctas);
   const int64_t ctas_res = ctas_1 / num_n * num_n;
-  const bool res_possible = path != GEMM_PATH_PAIR && !b_kn && num_n <= kMaxResidentN &&
+  const bool res_possible = !split_k && path != GEMM_PATH_PAIR && !b_kn && num_n <= kMaxResidentN &&
                             ctas_res >= 1 && (num_n == 1 || o.group_m <= 1);
   if (o.b_resident == 2 && !res_possible) return GEMM_ERR_INVALID_VALUE;
   if (res_possible && (o.b_resident == 2 || (o.b_resident == 0 && tiles >= 2 * sms))) {
@@ -254,7 +312,8 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   // warps.
   int64_t ctas_cap = sms;
   if (o.max_ctas) ctas_cap = std::min<int64_t>(ctas_cap, o.max_ctas);
-  const bool small_possible = path == GEMM_PATH_SKINNY && !b_resident && num_n <= ctas_cap &&
+  const bool small_possible = !split_k && path == GEMM_PATH_SKINNY && !b_resident &&
+                              num_n <= ctas_cap &&
                               (o.epi_warps == 0 || o.epi_warps == kSkinnyEpiWarps);
   if (o.small_m == 2 && !small_possible) return GEMM_ERR_INVALID_VALUE;
   const bool small_m = small_possible && o.small_m != 1;
@@ -262,12 +321,20 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
     epi_warps = kSkinnyEpiWarps;
     katoms = o.katoms ? o.katoms : kSkinnyKatoms;
   }
+  if (split_k) {
+    epi_warps = kSplitEpiWarps;
+    katoms = split_katoms;
+  }
   const int64_t num_k = (K + kBK * katoms - 1) / (kBK * katoms);
   uint32_t stage_bytes = b_resident ? static_cast<uint32_t>(katoms) * kABytes
                                     : stage_bytes_for(path, bn, katoms, nt);
   int stages = 0;
   uint32_t smem_total = 0;
-  if (small_m) {
+  if (split_k) {
+    stage_bytes = split_stage_bytes;
+    stages = split_stages;
+    smem_total = SplitLayout::make(stages, stage_bytes).total + 1024;
+  } else if (small_m) {
     const auto small_total = [&](int sc) { return SkinnyLayout::make(sc, stage_bytes).total + 1024; };
     int fit = 1;
     while (fit + 1 <= kMaxStages && small_total(fit + 1) <= static_cast<uint32_t>(kMaxDynSmem))
@@ -296,7 +363,9 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
     return std::min<int64_t>(slots, (even + multiple - 1) / multiple * multiple);
   };
   int ctas;
-  if (small_m) {
+  if (split_k) {
+    ctas = static_cast<int>(2 * tiles);  // a CTA pair for each tile
+  } else if (small_m) {
     ctas = static_cast<int>(tiles);  // one tile each
   } else if (path == GEMM_PATH_PAIR) {
     int64_t pairs = std::min<int64_t>(units, max_pairs);
@@ -325,11 +394,12 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   pl.cfg.tiles = static_cast<int>(tiles);
   pl.cfg.smem_bytes = static_cast<int>(smem_total);  // includes 1 KiB of alignment slack
   // two accumulators (consecutive tiles overlap), one in the small-M kernel
-  pl.cfg.tmem_cols = static_cast<int>(pow2_at_least(small_m ? bn : 2u * bn));
+  pl.cfg.tmem_cols = static_cast<int>(pow2_at_least((small_m || split_k) ? bn : 2u * bn));
   pl.cfg.b_resident = b_resident ? 1 : 0;
   pl.cfg.pdl = o.pdl ? 0 : 1;
   pl.cfg.wide = wide ? 1 : 0;
   pl.cfg.small_m = small_m ? 1 : 0;
+  pl.cfg.split_k = split_k ? 1 : 0;
 
   GemmParams& p = pl.p;
   p.M = static_cast<int32_t>(M);
@@ -388,7 +458,7 @@ bool grant_smem(Kernel k) {
 // x scaled epilogue for the pair.
 template <bool kDirectD>
 bool grant_all(bool ok) {
-  return ok && grant_smem(gemm_tn_f16_skinny<kDirectD>) &&
+  return ok && grant_smem(gemm_tn_f16_skinny<kDirectD>) && grant_smem(gemm_tn_f16_splitk) &&
          grant_smem(gemm_tn_f16_persistent<4, false, kDirectD>) &&
          grant_smem(gemm_tn_f16_persistent<8, false, kDirectD>) &&
          grant_smem(gemm_tn_f16_persistent<4, true, kDirectD>) &&
@@ -563,7 +633,7 @@ int launch_gemm(int64_t M, int64_t N, int64_t K, const View& a, const View& b, c
   int rc;
   if ((rc = prepare_device(st)) != GEMM_OK) return rc;
   Plan pl;
-  rc = make_plan(M, N, K, opt, st->sm_count, st->max_pairs, &pl, b_kn);
+  rc = make_plan(M, N, K, opt, st->sm_count, st->max_pairs, &pl, b_kn, d_direct != nullptr);
   if (rc != GEMM_OK) return rc;
   if ((rc = get_encoder()) != GEMM_OK) return rc;
   pl.p.ldc = ldc;
@@ -601,7 +671,7 @@ int launch_gemm(int64_t M, int64_t N, int64_t K, const View& a, const View& b, c
     attr[nattr].val.programmaticStreamSerializationAllowed = 1;
     ++nattr;
   }
-  if (pair) {
+  if (pair || pl.cfg.split_k) {
     attr[nattr].id = cudaLaunchAttributeClusterDimension;
     attr[nattr].val.clusterDim.x = 2;
     attr[nattr].val.clusterDim.y = 1;
@@ -616,6 +686,7 @@ int launch_gemm(int64_t M, int64_t N, int64_t K, const View& a, const View& b, c
   cfg.numAttrs = nattr;
   const bool wide = pl.cfg.wide != 0, res = pl.p.b_resident != 0, small = pl.cfg.small_m != 0;
   const cudaError_t e =
+      pl.cfg.split_k ? cudaLaunchKernelEx(&cfg, gemm_tn_f16_splitk, tmA, tmB, tmD, pl.p) :
       d_direct ? launch_kernel<true>(cfg, pair, wide, res, small, pl.cfg.epi_warps, tmA, tmB, tmD,
                                      pl.p)
                : launch_kernel<false>(cfg, pair, wide, res, small, pl.cfg.epi_warps, tmA, tmB,

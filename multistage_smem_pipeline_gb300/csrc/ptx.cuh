@@ -293,6 +293,29 @@ __device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t cluster_a
       : "memory");
 }
 
+// True once the phase with the given parity has completed, with acquire
+// semantics at cluster scope: writes that other CTAs of the cluster made
+// before their release-arrives on this barrier are visible afterwards.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// 16-byte store to a shared::cluster address (another CTA's shared memory).
+__device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, uint32_t a, uint32_t b,
+                                              uint32_t c, uint32_t d) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "r"(a),
+               "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
 // TMA load into this CTA's shared memory whose byte count completes on an
 // mbarrier that may live in either CTA of the pair.
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap,

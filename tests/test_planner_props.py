@@ -33,13 +33,19 @@ def _check(cfg, M, N, K):
     assert cfg["epi_warps"] in (4, 8)
     assert 32 <= cfg["bn"] <= 256 and cfg["bn"] % 32 == 0
     # two accumulators, or one in the small-M kernel (one tile per CTA)
-    accs = 1 if cfg["small_m"] else 2
+    accs = 1 if (cfg["small_m"] or cfg["split_k"]) else 2
     assert cfg["tmem_cols"] >= accs * cfg["bn"] and cfg["tmem_cols"] <= TMEM_COLS
     assert cfg["tmem_cols"] & (cfg["tmem_cols"] - 1) == 0          # a power of two
     bm = 256 if cfg["path"] == 3 else 128
     assert cfg["bm"] == bm
     assert cfg["tiles"] == -(-M // bm) * -(-N // cfg["bn"])
-    assert 1 <= cfg["ctas"] <= cfg["tiles"] * (2 if cfg["path"] == 3 else 1)
+    assert 1 <= cfg["ctas"] <= cfg["tiles"] * (2 if (cfg["path"] == 3 or cfg["split_k"]) else 1)
+    if cfg["split_k"]:
+        assert cfg["ctas"] == 2 * cfg["tiles"] and cfg["bn"] % 64 == 0 and cfg["path"] == 1
+        assert cfg["epi_warps"] == 4 and not cfg["b_resident"] and not cfg["small_m"]
+        # the ring holds the exchange: 16 KiB of staging and the peer's 128 x bn/2 fp32 partial
+        ring = cfg["kstage"] * cfg["katoms"] * (128 + cfg["bn"]) * 128
+        assert ring >= 16384 + 256 * cfg["bn"]
     if cfg["path"] == 3:
         assert cfg["ctas"] % 2 == 0                                    # whole clusters of 2
     if cfg["path"] == 2:
@@ -60,6 +66,8 @@ def _check(cfg, M, N, K):
         num_n = -(-N // cfg["bn"])
         work = -(-M // 256) * (-(-num_n // 2) if cfg["wide"] else num_n)
         slots, step = cfg["ctas"] // 2, 1
+    elif cfg["split_k"]:
+        work, slots, step = cfg["tiles"], cfg["ctas"] // 2, 1
     else:
         work, slots = cfg["tiles"], cfg["ctas"]
         step = -(-N // cfg["bn"]) if cfg["b_resident"] else 1
@@ -77,7 +85,8 @@ def test_default_plans_fit(binding):
                                   dict(acc_f16=1), dict(b_layout=1), dict(max_ctas=37),
                                   dict(wide=2), dict(wide=2, path=3, epi_warps=8),
                                   dict(wide=1), dict(small_m=1), dict(small_m=2),
-                                  dict(small_m=2, katoms=1)])
+                                  dict(small_m=2, katoms=1), dict(split_k=1), dict(split_k=2),
+                                  dict(split_k=2, katoms=1), dict(split_k=2, bn=256)])
 def test_forced_plans_fit_or_are_refused(binding, opts):
     accepted = 0
     for M, N, K in _shapes(600, 502 + len(str(opts))):
@@ -100,6 +109,8 @@ def test_forced_plans_fit_or_are_refused(binding, opts):
             assert cfg["wide"] == 1
         if opts.get("wide") == 1:
             assert cfg["wide"] == 0
+        if "split_k" in opts:
+            assert cfg["split_k"] == (1 if opts["split_k"] == 2 else 0)
         if "small_m" in opts:
             assert cfg["small_m"] == (1 if opts["small_m"] == 2 else 0)
         if opts.get("b_resident") == 1:

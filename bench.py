@@ -75,7 +75,7 @@ def load_peaks():
 # The sources that decide the GEMM kernel's code and its launch plan: the
 # recorded DRAM traffic stays valid while these are unchanged.
 KERNEL_SOURCES = ("ptx.cuh", "pipeline.cuh", "gemm_kernel.cuh", "gemm_pair_kernel.cuh",
-                  "gemm_skinny_kernel.cuh", "gemm_tn_f16.cu")
+                  "gemm_skinny_kernel.cuh", "gemm_splitk_kernel.cuh", "gemm_tn_f16.cu")
 
 
 def code_tokens(text: str) -> str:
@@ -609,7 +609,7 @@ def bench_config(tag, binding, torch, dev, stream, l2, peaks, peak_src, clocks):
              "roofline_ms": max(flops / (float(peaks["bf16_tflops"]) * 1e12),
                                 alg_bytes / (float(peaks["hbm_gbs"]) * 1e9)) * 1e3,
              "plan": {k: cfg[k] for k in ("path", "bn", "kstage", "katoms", "ctas", "epi_warps",
-                                          "b_resident", "wide", "small_m")},
+                                          "b_resident", "wide", "small_m", "split_k")},
              "l2": f"{R} operand copies ({R * int(alg_bytes) >> 20} MiB > 3 x L2) cycled",
              "clocks": clk}
     entry["roofline_frac"] = entry["roofline_ms"] / ms
@@ -676,7 +676,7 @@ def run_gpu(args, tag):
     opts = {"path": ["auto", "square", "skinny", "pair"].index(args.path), "bn": args.bn,
             "kstage": args.kstage, "katoms": args.katoms, "group_m": args.group_m,
             "epi_warps": args.epi_warps, "b_resident": args.b_resident, "pdl": args.pdl,
-            "wide": args.wide, "small_m": args.small_m}
+            "wide": args.wide, "small_m": args.small_m, "split_k": args.split_k}
     forced = any(opts.values())
     cfg = binding.query_config(M, N, K, b_layout=1 if spec.get("b_kn") else 0,
                                acc_f16=1 if spec.get("acc_f16") else 0, **opts)
@@ -935,6 +935,7 @@ def run_gpu(args, tag):
                                                             2 if cfg["wide"] else 1,
                                                             flag(scaled))
                       if cfg["path"] == 3 else
+                      "gemm_tn_f16_splitk" if cfg["split_k"] else
                       "gemm_tn_f16_skinny<%s>" % flag(direct_d) if cfg["small_m"] else
                       "gemm_tn_f16_persistent<%d, %s, %s>" % (cfg["epi_warps"],
                                                               flag(cfg["b_resident"]),
@@ -967,7 +968,7 @@ def run_gpu(args, tag):
                 "bn": cfg["bn"], "bk": cfg["bk"], "kstage": cfg["kstage"], "ctas": cfg["ctas"],
                 "tiles": cfg["tiles"], "katoms": cfg["katoms"], "epi_warps": cfg["epi_warps"],
                 "b_resident": cfg["b_resident"], "pdl": cfg["pdl"], "wide": cfg["wide"],
-                "small_m": cfg["small_m"], "forced": forced}),
+                "small_m": cfg["small_m"], "split_k": cfg["split_k"], "forced": forced}),
             "launch_ms": ({"mean": ms, "median": statistics.median(launches_ms),
                            "p10": float(np.percentile(launches_ms, 10)),
                            "p90": float(np.percentile(launches_ms, 90))}
@@ -1052,6 +1053,8 @@ def main():
                     help="diagnostics: 1 = launch without programmatic dependent launch")
     ap.add_argument("--wide", type=int, default=0, choices=[0, 1, 2],
                     help="diagnostics: pair units of two n-tiles (0 choose, 1 never, 2 always)")
+    ap.add_argument("--split-k", type=int, default=0, choices=[0, 1, 2],
+                    help="diagnostics: k split over a CTA pair (0 choose, 1 never, 2 always)")
     ap.add_argument("--small-m", type=int, default=0, choices=[0, 1, 2],
                     help="diagnostics: the small-M kernel, one tile per CTA (0 choose, 1 never, "
                          "2 always)")

@@ -14,42 +14,39 @@
 // operands and 32 MMAs per CTA instead of 384 KiB and 64 for a 128 x 64 tile
 // over the whole k range -- for a 32 KiB exchange.
 //
-// The exchange reuses the ring: once a CTA's MMAs have completed, nothing
-// fills or reads its ring any more (one tile per cluster), so the epilogue's
-// staging buffers take its first 16 KiB and the peer's partial the next
-// 128 x BN/2 x 4 bytes.  Two barriers per CTA order it, each completed by
-// the 128 epilogue threads of the peer with release at cluster scope and
-// waited on with acquire at cluster scope:
-//   peer_free  -- "my MMAs are done, you may write into my ring";
-//   rx_full    -- "my partial of your half is in your ring".
-// The final value of an element is p0 + p1 in fp32 whichever CTA forms it,
-// so the result does not depend on the pair's timing.  Every wait is
-// bounded; both CTAs meet on a cluster barrier before either exits.
+// The peer's partial lands in a region of its own after the ring
+// (128 x BN/2 x 4 bytes), so a CTA may send as soon as its own MMAs are done,
+// without waiting for the peer's; one barrier per CTA, completed by the 256
+// epilogue threads of the peer with release at cluster scope and waited on
+// with acquire at cluster scope, says that the partial has arrived.  The
+// epilogue's staging buffers reuse the ring, idle once the CTA's MMAs have
+// completed (one tile per pair).  Eight epilogue warps, two per TMEM lane
+// quadrant, each send and finish every other 32-column chunk.  The final
+// value of an element is p0 + p1 in fp32 whichever CTA forms it, so the
+// result does not depend on the pair's timing.  Every wait is bounded; both
+// CTAs meet on a cluster barrier before either exits.
 #pragma once
 #include "gemm_kernel.cuh"
 
 namespace gb300 {
 
-constexpr int kSplitEpiWarps = 4;
+constexpr int kSplitEpiWarps = 8;
 constexpr int kSplitThreads = 64 + 32 * kSplitEpiWarps;  // producer, MMA, epilogue
 constexpr int kSplitPeerArrivals = 32 * kSplitEpiWarps;   // the peer's epilogue threads
-constexpr uint32_t kSplitStagingBytes = kSplitEpiWarps * kEpiBufs * kEpiChunkBytes;  // 16 KiB
+constexpr uint32_t kSplitStagingBytes = kSplitEpiWarps * kEpiBufs * kEpiChunkBytes;  // 32 KiB
 
-// Bytes the ring must hold for the exchange: the staging buffers, then the
-// peer's fp32 partial of this CTA's BN/2 columns.
-__host__ __device__ constexpr uint32_t splitk_exchange_bytes(int bn) {
-  return kSplitStagingBytes + static_cast<uint32_t>(bn) * 256u;
-}
-
-// Shared-memory carve-up, offsets from the 1024-aligned base: the ring, then
-// the mbarriers full[S], empty[S], tmem-full, drain, peer-free, rx-full.
+// Shared-memory carve-up, offsets from the 1024-aligned base: the ring (whose
+// first 32 KiB the epilogue's staging buffers reuse), the peer's fp32 partial
+// of this CTA's BN/2 columns, then the mbarriers full[S], empty[S],
+// tmem-full, drain, rx-full.
 struct SplitLayout {
-  uint32_t ring, bars, misc, total;
-  __host__ __device__ static SplitLayout make(int stages, uint32_t stage_bytes) {
+  uint32_t ring, rx, bars, misc, total;
+  __host__ __device__ static SplitLayout make(int stages, uint32_t stage_bytes, int bn) {
     SplitLayout L;
     L.ring = 0;
-    L.bars = stages * stage_bytes;
-    L.misc = L.bars + 8 * (2 * stages + 4);
+    L.rx = stages * stage_bytes;
+    L.bars = L.rx + static_cast<uint32_t>(bn) * 256u;
+    L.misc = L.bars + 8 * (2 * stages + 3);
     L.total = L.misc + 16;
     return L;
   }
@@ -91,7 +88,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* const smem = smem_raw + (base - raw);
   const int S = p.stages;
-  const SplitLayout L = SplitLayout::make(S, p.stage_bytes);
+  const SplitLayout L = SplitLayout::make(S, p.stage_bytes, p.bn);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -108,8 +105,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
   auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
   const uint32_t tfull_bar = bars + 8u * (2 * S);
   const uint32_t drain_bar = bars + 8u * (2 * S + 1);
-  const uint32_t peer_free_bar = bars + 8u * (2 * S + 2);
-  const uint32_t rx_full_bar = bars + 8u * (2 * S + 3);
+  const uint32_t rx_full_bar = bars + 8u * (2 * S + 2);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc + 4);
 
@@ -121,7 +117,6 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     }
     mbar_init(tfull_bar, 1);
     mbar_init(drain_bar, 1);
-    mbar_init(peer_free_bar, kSplitPeerArrivals);
     mbar_init(rx_full_bar, kSplitPeerArrivals);
     *abort_flag = 0;
     fence_barrier_init();
@@ -208,15 +203,15 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
       wait_timed(drain_bar, 0, p.timeout_ns);
     }
   } else {
-    // ------------------------------------------------------------ epilogue (warps 2..5)
-    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    // ------------------------------------------------------------ epilogue (warps 2..9)
+    const int q = warp & 3;            // TMEM lane quadrant this warp may access
+    const int sel = (warp - 2) >> 2;   // which of every two 32-column chunks it takes
     const int row = q * 32 + lane;
     const int m0 = mb * kBM + q * 32;
     const bool rows_live = m0 < p.M;
     const int half = p.bn / 2;  // a multiple of 32
-    const uint32_t ring = base + L.ring;
-    const uint32_t my_bufs = ring + (warp - 2) * kEpiBufs * kEpiChunkBytes;
-    const uint32_t rx = ring + kSplitStagingBytes;
+    const uint32_t my_bufs = base + L.ring + (warp - 2) * kEpiBufs * kEpiChunkBytes;
+    const uint32_t rx = base + L.rx;
     const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     int ok = 0;
     if (lane == 0) ok = wait_or_abort(tfull_bar, 0, p.timeout_ns, abort_flag, kSiteTmemFull);
@@ -224,69 +219,65 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     if (ok) {
       tc_fence_after_sync();
       fence_proxy_async_smem();  // the ring's last async-proxy uses precede the writes below
-      // 1. this CTA's MMAs are done: the peer may write into its ring
-      mbar_arrive_cluster(mapa_shared(peer_free_bar, peer));
-      // 2. once the peer's are done too, send it this CTA's partial of its half
-      // (every thread acquires the peer's arrivals; the warp goes on only if
-      // all did, so the tcgen05.ld below stays warp-uniform)
-      if (__all_sync(0xffffffffu, wait_cluster_or_abort(peer_free_bar, 0, p.timeout_ns,
-                                                        abort_flag, kSiteTmemFull))) {
-        if (rows_live) {
-          const uint32_t peer_rx = mapa_shared(rx, peer);
-          for (int c = 0; c < half / kEpiCols; ++c) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(peer * half + c * kEpiCols), r);
-            tmem_ld_wait();
+      // 1. send this CTA's partial of the peer's half into the peer's region
+      if (rows_live) {
+        const uint32_t peer_rx = mapa_shared(rx, peer);
+        for (int c = sel; c < half / kEpiCols; c += 2) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(peer * half + c * kEpiCols), r);
+          tmem_ld_wait();
 #pragma unroll
-            for (int g = 0; g < 8; ++g)
-              st_cluster_v4(peer_rx + splitk_rx_offset(c * 8 + g, row), r[4 * g], r[4 * g + 1],
-                            r[4 * g + 2], r[4 * g + 3]);
-          }
+          for (int g = 0; g < 8; ++g)
+            st_cluster_v4(peer_rx + splitk_rx_offset(c * 8 + g, row), r[4 * g], r[4 * g + 1],
+                          r[4 * g + 2], r[4 * g + 3]);
         }
-        // release: this thread's stores above are visible to the peer's acquire
-        mbar_arrive_cluster(mapa_shared(rx_full_bar, peer));
-        // 3. the peer's partial of this CTA's half: add, round, store
-        if (__all_sync(0xffffffffu, wait_cluster_or_abort(rx_full_bar, 0, p.timeout_ns,
-                                                          abort_flag, kSiteTmemFull)) &&
-            rows_live) {
-          const int n0 = nb * p.bn + static_cast<int>(rank) * half;
-          const int nchunks = (min(half, p.N - n0) + kEpiCols - 1) / kEpiCols;
-          for (int c = 0; c < nchunks; ++c) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(rank * half + c * kEpiCols), r);
-            tmem_ld_wait();
+      }
+      // release: this thread's stores above are visible to the peer's acquire
+      mbar_arrive_cluster(mapa_shared(rx_full_bar, peer));
+      // 2. the peer's partial of this CTA's half: add, round, store (every
+      // thread acquires the peer's arrivals; the warp goes on only if all
+      // did, so the tcgen05.ld below stays warp-uniform)
+      if (__all_sync(0xffffffffu, wait_cluster_or_abort(rx_full_bar, 0, p.timeout_ns, abort_flag,
+                                                        kSiteTmemFull)) &&
+          rows_live) {
+        const int n0 = nb * p.bn + static_cast<int>(rank) * half;
+        const int nchunks = (min(half, p.N - n0) + kEpiCols - 1) / kEpiCols;
+        int seq = 0;
+        for (int c = sel; c < nchunks; c += 2, ++seq) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(rank * half + c * kEpiCols), r);
+          tmem_ld_wait();
 #pragma unroll
-            for (int g = 0; g < 8; ++g) {
-              const uint4 v = ld_shared_v4(rx + splitk_rx_offset(c * 8 + g, row));
-              r[4 * g] = __float_as_uint(__uint_as_float(r[4 * g]) + __uint_as_float(v.x));
-              r[4 * g + 1] = __float_as_uint(__uint_as_float(r[4 * g + 1]) + __uint_as_float(v.y));
-              r[4 * g + 2] = __float_as_uint(__uint_as_float(r[4 * g + 2]) + __uint_as_float(v.z));
-              r[4 * g + 3] = __float_as_uint(__uint_as_float(r[4 * g + 3]) + __uint_as_float(v.w));
-            }
-            const uint32_t buf = my_bufs + (c % kEpiBufs) * kEpiChunkBytes;
-            if (c >= kEpiBufs) {
-              if (lane == 0) bulk_wait_group_read<kEpiBufs - 1>();
-              __syncwarp();
-            }
-            if (p.scaled) {
-              const bool with_c = p.beta != 0.0f;
-              if (with_c) stage_c_chunk(p, m0, n0 + c * kEpiCols, lane, buf);
-              apply_alpha_beta(r, p, with_c, buf, lane);
-            }
-            const uint32_t row_addr = buf + lane * 64u;
-            const uint32_t sw = (lane >> 1) & 3u;
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              st_shared_v4(row_addr + ((j ^ sw) << 4), pack_half2(r[8 * j + 0], r[8 * j + 1]),
-                           pack_half2(r[8 * j + 2], r[8 * j + 3]),
-                           pack_half2(r[8 * j + 4], r[8 * j + 5]),
-                           pack_half2(r[8 * j + 6], r[8 * j + 7]));
-            fence_proxy_async_smem();
+          for (int g = 0; g < 8; ++g) {
+            const uint4 v = ld_shared_v4(rx + splitk_rx_offset(c * 8 + g, row));
+            r[4 * g] = __float_as_uint(__uint_as_float(r[4 * g]) + __uint_as_float(v.x));
+            r[4 * g + 1] = __float_as_uint(__uint_as_float(r[4 * g + 1]) + __uint_as_float(v.y));
+            r[4 * g + 2] = __float_as_uint(__uint_as_float(r[4 * g + 2]) + __uint_as_float(v.z));
+            r[4 * g + 3] = __float_as_uint(__uint_as_float(r[4 * g + 3]) + __uint_as_float(v.w));
+          }
+          const uint32_t buf = my_bufs + (seq % kEpiBufs) * kEpiChunkBytes;
+          if (seq >= kEpiBufs) {
+            if (lane == 0) bulk_wait_group_read<kEpiBufs - 1>();
             __syncwarp();
-            if (lane == 0) {
-              tma_store_2d(&tmD, buf, n0 + c * kEpiCols, m0);
-              bulk_commit_group();
-            }
+          }
+          if (p.scaled) {
+            const bool with_c = p.beta != 0.0f;
+            if (with_c) stage_c_chunk(p, m0, n0 + c * kEpiCols, lane, buf);
+            apply_alpha_beta(r, p, with_c, buf, lane);
+          }
+          const uint32_t row_addr = buf + lane * 64u;
+          const uint32_t sw = (lane >> 1) & 3u;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            st_shared_v4(row_addr + ((j ^ sw) << 4), pack_half2(r[8 * j + 0], r[8 * j + 1]),
+                         pack_half2(r[8 * j + 2], r[8 * j + 3]),
+                         pack_half2(r[8 * j + 4], r[8 * j + 5]),
+                         pack_half2(r[8 * j + 6], r[8 * j + 7]));
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmD, buf, n0 + c * kEpiCols, m0);
+            bulk_commit_group();
           }
         }
       }

@@ -219,7 +219,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
         const uint32_t b = static_cast<uint32_t>(k2) * (kABytes + static_cast<uint32_t>(cand) * 128u);
         int f = 1;
         while (f + 1 <= kMaxStages &&
-               SplitLayout::make(f + 1, b).total + 1024 <= static_cast<uint32_t>(kMaxDynSmem))
+               SplitLayout::make(f + 1, b, cand).total + 1024 <= static_cast<uint32_t>(kMaxDynSmem))
           ++f;
         if (k2 == 2 && !o.katoms && f < 3) continue;
         ka = k2;
@@ -227,25 +227,30 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
         sb = b;
       }
       // this is the tile width; the plan stands or falls with it
-      const int st = o.kstage ? o.kstage : fit;
       if (!ka || (K + kBK * ka - 1) / (kBK * ka) < 2 ||  // a k-block for each CTA at least
-          st < 2 || st > fit || st * sb < splitk_exchange_bytes(cand))
+          fit < 2 || fit * sb < kSplitStagingBytes)
         break;
       split_bn = cand;
       split_katoms = ka;
-      split_stages = st;
+      split_stages = fit;
       split_stage_bytes = sb;
     }
   }
   if (o.split_k == 2 && !split_bn) return GEMM_ERR_INVALID_VALUE;
   const bool split_k =
       split_bn && (o.split_k == 2 ||
-                   (o.split_k == 0 && path == GEMM_PATH_SQUARE && o.b_resident == 0 && M > kBM &&
-                    K >= 512 && K <= 1024 && tiles_1 <= sms));
+                   (o.split_k == 0 && o.path == GEMM_PATH_AUTO && path == GEMM_PATH_SQUARE &&
+                    o.b_resident == 0 && M > kBM && K >= 512 && K <= 1024 && tiles_1 <= sms));
   if (split_k) {
     bn = split_bn;
     path = GEMM_PATH_SQUARE;
     nt = 1;
+    if (o.kstage) {  // a forced ring depth must fit this kernel's plan
+      if (o.kstage > split_stages ||
+          static_cast<uint32_t>(o.kstage) * split_stage_bytes < kSplitStagingBytes)
+        return GEMM_ERR_INVALID_VALUE;
+      split_stages = o.kstage;
+    }
   }
 
   const int bm = (path == GEMM_PATH_PAIR) ? 2 * kBM : kBM;
@@ -333,7 +338,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   if (split_k) {
     stage_bytes = split_stage_bytes;
     stages = split_stages;
-    smem_total = SplitLayout::make(stages, stage_bytes).total + 1024;
+    smem_total = SplitLayout::make(stages, stage_bytes, bn).total + 1024;
   } else if (small_m) {
     const auto small_total = [&](int sc) { return SkinnyLayout::make(sc, stage_bytes).total + 1024; };
     int fit = 1;

@@ -42,10 +42,11 @@ def _check(cfg, M, N, K):
     assert 1 <= cfg["ctas"] <= cfg["tiles"] * (2 if (cfg["path"] == 3 or cfg["split_k"]) else 1)
     if cfg["split_k"]:
         assert cfg["ctas"] == 2 * cfg["tiles"] and cfg["bn"] % 64 == 0 and cfg["path"] == 1
-        assert cfg["epi_warps"] == 4 and not cfg["b_resident"] and not cfg["small_m"]
-        # the ring holds the exchange: 16 KiB of staging and the peer's 128 x bn/2 fp32 partial
+        assert cfg["epi_warps"] == 8 and not cfg["b_resident"] and not cfg["small_m"]
+        # the ring holds the eight warps' staging buffers once the MMAs are done, and the
+        # peer's 128 x bn/2 fp32 partial has a region of its own
         ring = cfg["kstage"] * cfg["katoms"] * (128 + cfg["bn"]) * 128
-        assert ring >= 16384 + 256 * cfg["bn"]
+        assert ring >= 32768 and cfg["smem_bytes"] >= ring + 256 * cfg["bn"]
     if cfg["path"] == 3:
         assert cfg["ctas"] % 2 == 0                                    # whole clusters of 2
     if cfg["path"] == 2:

@@ -59,6 +59,11 @@ def test_shapes_with_tails(lib, gpu, M, N, K):
 @pytest.mark.parametrize("bn", [64, 128, 192, 256])
 @pytest.mark.parametrize("katoms", [1, 2])
 def test_tile_widths_and_slices(lib, gpu, bn, katoms):
+    if bn == 256 and katoms == 2:
+        # two 96 KiB stages and the 64 KiB region for the peer's partial do not fit
+        with pytest.raises(lib.GemmError):
+            lib.query_config(520, 600, 776, split_k=2, bn=bn, katoms=katoms)
+        return
     a = synthetic.gaussian(bn + katoms, (520, 776))
     b = synthetic.gaussian(bn + katoms + 1, (600, 776))
     _check(_run(lib, a, b, gpu, split_k=2, bn=bn, katoms=katoms), a, b)

@@ -16,11 +16,12 @@
 //
 // The peer's partial lands in a region of its own after the ring
 // (128 x BN/2 x 4 bytes), so a CTA may send as soon as its own MMAs are done,
-// without waiting for the peer's; one barrier per CTA, completed by the 256
-// epilogue threads of the peer with release at cluster scope and waited on
-// with acquire at cluster scope, says that the partial has arrived.  The
-// epilogue's staging buffers reuse the ring, idle once the CTA's MMAs have
-// completed (one tile per pair).  Eight epilogue warps, two per TMEM lane
+// without waiting for the peer's.  Each epilogue warp writes its 32 x 32
+// chunk of the peer's half into its own ring (idle once the CTA's MMAs have
+// completed: one tile per pair) and one lane moves it with a bulk copy into
+// the peer's region, whose bytes complete on the peer's receive barrier (one
+// expect_tx of the whole half, made at set-up).  The epilogue's staging
+// buffers for D also reuse the ring.  Eight epilogue warps, two per TMEM lane
 // quadrant, each send and finish every other 32-column chunk.  The final
 // value of an element is p0 + p1 in fp32 whichever CTA forms it, so the
 // result does not depend on the pair's timing.  Every wait is bounded; both
@@ -32,13 +33,17 @@ namespace gb300 {
 
 constexpr int kSplitEpiWarps = 8;
 constexpr int kSplitThreads = 64 + 32 * kSplitEpiWarps;  // producer, MMA, epilogue
-constexpr int kSplitPeerArrivals = 32 * kSplitEpiWarps;   // the peer's epilogue threads
 constexpr uint32_t kSplitStagingBytes = kSplitEpiWarps * kEpiBufs * kEpiChunkBytes;  // 32 KiB
 
-// Shared-memory carve-up, offsets from the 1024-aligned base: the ring (whose
-// first 32 KiB the epilogue's staging buffers reuse), the peer's fp32 partial
-// of this CTA's BN/2 columns, then the mbarriers full[S], empty[S],
-// tmem-full, drain, rx-full.
+// Bytes of ring the epilogue reuses: the staging buffers for D, then this
+// CTA's partial of the peer's half on its way out.
+__host__ __device__ constexpr uint32_t splitk_ring_reuse_bytes(int bn) {
+  return kSplitStagingBytes + static_cast<uint32_t>(bn) * 256u;
+}
+
+// Shared-memory carve-up, offsets from the 1024-aligned base: the ring (see
+// splitk_ring_reuse_bytes), the peer's fp32 partial of this CTA's BN/2
+// columns, then the mbarriers full[S], empty[S], tmem-full, drain, rx-full.
 struct SplitLayout {
   uint32_t ring, rx, bars, misc, total;
   __host__ __device__ static SplitLayout make(int stages, uint32_t stage_bytes, int bn) {
@@ -71,12 +76,13 @@ __device__ __forceinline__ bool wait_cluster_or_abort(uint32_t bar, uint32_t par
   }
 }
 
-// The peer's partial of this CTA's half, 128 rows x BN/2 fp32 columns, as
-// 16-byte groups: group g (columns 4g..4g+3 of the half) of row `row` at
-// (g * 128 + row) * 16, so a warp's 32 rows of one group are 512 contiguous
-// bytes for both the peer's stores and this CTA's loads.
-__device__ __forceinline__ uint32_t splitk_rx_offset(int g, int row) {
-  return static_cast<uint32_t>(g * 128 + row) * 16u;
+// A partial of half a tile, 128 rows x BN/2 fp32 columns, as the epilogue
+// warps hold it: chunk c (32 columns) of lane quadrant q is 4 KiB at
+// (c * 4 + q) * 4096, in which 16-byte group g (columns 4g..4g+3) of row
+// q * 32 + lane lies at g * 512 + lane * 16 -- one bulk copy per warp and
+// chunk, and conflict-free 16-byte stores and loads across a warp.
+__device__ __forceinline__ uint32_t splitk_chunk_offset(int c, int q) {
+  return static_cast<uint32_t>(c * 4 + q) * 4096u;
 }
 
 __global__ void __launch_bounds__(kSplitThreads, 1)
@@ -117,7 +123,9 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     }
     mbar_init(tfull_bar, 1);
     mbar_init(drain_bar, 1);
-    mbar_init(rx_full_bar, kSplitPeerArrivals);
+    mbar_init(rx_full_bar, 1);
+    // the peer's bulk copies of this CTA's half complete these bytes
+    mbar_arrive_expect_tx(rx_full_bar, static_cast<uint32_t>(p.bn) * 256u);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -206,7 +214,6 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     // ------------------------------------------------------------ epilogue (warps 2..9)
     const int q = warp & 3;            // TMEM lane quadrant this warp may access
     const int sel = (warp - 2) >> 2;   // which of every two 32-column chunks it takes
-    const int row = q * 32 + lane;
     const int m0 = mb * kBM + q * 32;
     const bool rows_live = m0 < p.M;
     const int half = p.bn / 2;  // a multiple of 32
@@ -219,24 +226,32 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     if (ok) {
       tc_fence_after_sync();
       fence_proxy_async_smem();  // the ring's last async-proxy uses precede the writes below
-      // 1. send this CTA's partial of the peer's half into the peer's region
-      if (rows_live) {
-        const uint32_t peer_rx = mapa_shared(rx, peer);
-        for (int c = sel; c < half / kEpiCols; c += 2) {
+      // 1. send this CTA's partial of the peer's half: through this CTA's idle
+      // ring, one bulk copy per warp and chunk into the peer's region
+      const uint32_t out = base + L.ring + kSplitStagingBytes;
+      for (int c = sel; c < half / kEpiCols; c += 2) {
+        const uint32_t off = splitk_chunk_offset(c, q);
+        if (rows_live) {
           uint32_t r[32];
           tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(peer * half + c * kEpiCols), r);
           tmem_ld_wait();
 #pragma unroll
           for (int g = 0; g < 8; ++g)
-            st_cluster_v4(peer_rx + splitk_rx_offset(c * 8 + g, row), r[4 * g], r[4 * g + 1],
-                          r[4 * g + 2], r[4 * g + 3]);
+            st_shared_v4(out + off + g * 512u + lane * 16u, r[4 * g], r[4 * g + 1], r[4 * g + 2],
+                         r[4 * g + 3]);
+        }
+        // rows past M send whatever the ring holds: the peer stores nothing there
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          bulk_copy_to_cluster(mapa_shared(rx + off, peer), out + off, 4096u,
+                               mapa_shared(rx_full_bar, peer));
+          bulk_commit_group();
         }
       }
-      // release: this thread's stores above are visible to the peer's acquire
-      mbar_arrive_cluster(mapa_shared(rx_full_bar, peer));
-      // 2. the peer's partial of this CTA's half: add, round, store (every
-      // thread acquires the peer's arrivals; the warp goes on only if all
-      // did, so the tcgen05.ld below stays warp-uniform)
+      // 2. the peer's partial of this CTA's half: add, round, store (the warp
+      // goes on only if every lane saw it land, so the tcgen05.ld below stays
+      // warp-uniform)
       if (__all_sync(0xffffffffu, wait_cluster_or_abort(rx_full_bar, 0, p.timeout_ns, abort_flag,
                                                         kSiteTmemFull)) &&
           rows_live) {
@@ -249,7 +264,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
           tmem_ld_wait();
 #pragma unroll
           for (int g = 0; g < 8; ++g) {
-            const uint4 v = ld_shared_v4(rx + splitk_rx_offset(c * 8 + g, row));
+            const uint4 v = ld_shared_v4(rx + splitk_chunk_offset(c, q) + g * 512u + lane * 16u);
             r[4 * g] = __float_as_uint(__uint_as_float(r[4 * g]) + __uint_as_float(v.x));
             r[4 * g + 1] = __float_as_uint(__uint_as_float(r[4 * g + 1]) + __uint_as_float(v.y));
             r[4 * g + 2] = __float_as_uint(__uint_as_float(r[4 * g + 2]) + __uint_as_float(v.z));
@@ -283,12 +298,16 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
       }
     }
     if (lane == 0) bulk_wait_group_read<0>();
+    // After a timeout the peer's copies into this CTA may still be landing:
+    // give them a bounded wait before the shared memory is released (at once
+    // when the partial has arrived).
+    if (warp == 2 && lane == 0) wait_timed(rx_full_bar, 0, p.timeout_ns);
     __syncwarp();
   }
 
   __syncwarp();
   tc_fence_before_sync();
-  cluster_sync();  // no remote store or arrive targets a CTA that has left
+  cluster_sync();  // no copy or arrive targets a CTA that has left
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc(tmem_base, p.tmem_cols);

@@ -228,7 +228,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
       }
       // this is the tile width; the plan stands or falls with it
       if (!ka || (K + kBK * ka - 1) / (kBK * ka) < 2 ||  // a k-block for each CTA at least
-          fit < 2 || fit * sb < kSplitStagingBytes)
+          fit < 2 || fit * sb < splitk_ring_reuse_bytes(cand))
         break;
       split_bn = cand;
       split_katoms = ka;
@@ -247,7 +247,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
     nt = 1;
     if (o.kstage) {  // a forced ring depth must fit this kernel's plan
       if (o.kstage > split_stages ||
-          static_cast<uint32_t>(o.kstage) * split_stage_bytes < kSplitStagingBytes)
+          static_cast<uint32_t>(o.kstage) * split_stage_bytes < splitk_ring_reuse_bytes(bn))
         return GEMM_ERR_INVALID_VALUE;
       split_stages = o.kstage;
     }

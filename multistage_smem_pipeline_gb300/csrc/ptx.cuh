@@ -308,6 +308,17 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
   return ok != 0;
 }
 
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from
+// this CTA's shared memory to a shared::cluster address (another CTA's), the
+// bytes completing on an mbarrier given by its shared::cluster address.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster, uint32_t src,
+                                                     uint32_t bytes, uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst_cluster), "r"(src), "r"(bytes), "r"(bar_cluster)
+      : "memory");
+}
+
 // 16-byte store to a shared::cluster address (another CTA's shared memory).
 __device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, uint32_t a, uint32_t b,
                                               uint32_t c, uint32_t d) {

@@ -46,7 +46,7 @@ def _check(cfg, M, N, K):
         # the ring holds the eight warps' staging buffers once the MMAs are done, and the
         # peer's 128 x bn/2 fp32 partial has a region of its own
         ring = cfg["kstage"] * cfg["katoms"] * (128 + cfg["bn"]) * 128
-        assert ring >= 32768 and cfg["smem_bytes"] >= ring + 256 * cfg["bn"]
+        assert ring >= 32768 + 256 * cfg["bn"] and cfg["smem_bytes"] >= ring + 256 * cfg["bn"]
     if cfg["path"] == 3:
         assert cfg["ctas"] % 2 == 0                                    # whole clusters of 2
     if cfg["path"] == 2:

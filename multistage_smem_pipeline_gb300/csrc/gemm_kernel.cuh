@@ -12,7 +12,8 @@
 //                          take alternate 32-column chunks.
 // With one n-block (N <= BN) every tile multiplies by the same B; in the
 // resident-B mode the producer loads all of B (BN x K) once into its own
-// shared-memory region and the ring carries only A slices.
+// shared-memory region, each k-block behind its own barrier and issued with
+// the first tile's A stage that needs it, and the ring carries only A.
 //
 // This is the multistage pipeline of "cute(9) multistage_gemm" (sections 4-6:
 // a ring of kStage K-tiles, a prologue that runs ahead, a mainloop that
@@ -80,7 +81,8 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
   constexpr int kThreads = threads_for(kEpiWarps);
   constexpr int kChunkStride = kEpiWarps / 4;  // warps sharing a TMEM lane quadrant
   const SmemLayout L =
-      SmemLayout::make(p.stages, p.stage_bytes, kEpiWarps, kResident ? p.bres_bytes : 0u);
+      SmemLayout::make(p.stages, p.stage_bytes, kEpiWarps, kResident ? p.bres_bytes : 0u,
+                       kResident ? p.num_k_blocks : 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -91,7 +93,8 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
   auto tfull_bar = [&](int b) { return bars + 8u * (2 * S + b); };
   auto tempty_bar = [&](int b) { return bars + 8u * (2 * S + 2 + b); };
   const uint32_t drain_bar = bars + 8u * (2 * S + 4);
-  const uint32_t bres_bar = bars + 8u * (2 * S + 5);
+  // k-block j of the resident B completes on its own barrier
+  auto bres_bar = [&](int j) { return bars + 8u * (2 * S + 5 + j); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc + 4);
 
@@ -108,7 +111,9 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
       mbar_init(tempty_bar(b), kEpiWarps); // one arrive per epilogue warp
     }
     mbar_init(drain_bar, 1);
-    mbar_init(bres_bar, 1);  // producer's arrive.expect_tx for the resident B
+    if (kResident)
+      for (int j = 0; j < p.num_k_blocks; ++j)
+        mbar_init(bres_bar(j), 1);  // producer's arrive.expect_tx for k-block j of B
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -144,17 +149,13 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0;
-      if (kResident) {
-        // Every tile of this CTA multiplies by the same n-block of B (the host
-        // orders tiles n-fastest over a grid that is a multiple of num_n).
-        // Load all of its 64-wide K slices once, behind one barrier; the ring
-        // carries A only.
-        const int slices = p.num_k_blocks * p.katoms;
-        const int n_row = static_cast<int>(blockIdx.x % p.num_n_blocks) * p.bn;
-        mbar_arrive_expect_tx(bres_bar, p.bres_bytes);
-        for (int j = 0; j < slices; ++j)
-          tma_load_2d(base + L.bres + j * p.b_atom_bytes, &tmB, bres_bar, j * kBK, n_row);
-      }
+      // Resident B: every tile of this CTA multiplies by the same n-block of
+      // B (the host orders tiles n-fastest over a grid that is a multiple of
+      // num_n).  Its k-blocks are loaded once, during the first tile, each
+      // just before that tile's A stage for the same k-block and behind its
+      // own barrier, so the first MMAs need not wait for all of B.
+      const int n_row = static_cast<int>(blockIdx.x % p.num_n_blocks) * p.bn;
+      int b_issued = 0;
       for (int t = blockIdx.x; t < p.num_tiles && !*abort_flag; t += gridDim.x) {
         int mb, nb;
         tile_coords(t, p, mb, nb);
@@ -168,6 +169,13 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
           }
           const uint32_t a_dst = base + L.ring + stage * p.stage_bytes;
           const uint32_t b_dst = a_dst + p.katoms * kABytes;
+          if (kResident && t == static_cast<int>(blockIdx.x)) {  // B's k-block kb, once
+            mbar_arrive_expect_tx(bres_bar(kb), p.katoms * p.b_atom_bytes);
+            for (int at = 0; at < p.katoms; ++at)
+              tma_load_2d(base + L.bres + (kb * p.katoms + at) * p.b_atom_bytes, &tmB,
+                          bres_bar(kb), (kb * p.katoms + at) * kBK, n_row);
+            ++b_issued;
+          }
           mbar_arrive_expect_tx(full_bar(stage), p.stage_bytes);
           if (!(p.inject == 1 && issued == 0)) {
             for (int at = 0; at < p.katoms; ++at) {
@@ -203,7 +211,13 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
       const uint32_t first = issued > static_cast<uint32_t>(S) ? issued - S : 0u;
       for (uint32_t i = first; i < issued; ++i)
         wait_timed(full_bar(i % S), (i / S) & 1u, p.timeout_ns);
-      if (kResident) wait_timed(bres_bar, 0, p.timeout_ns);
+      if (kResident) {
+        const int kf = first_k_block(blockIdx.x, p);  // the first tile's k order
+        for (int j = 0; j < b_issued; ++j) {
+          const int kb = (kf + j < p.num_k_blocks) ? kf + j : kf + j - p.num_k_blocks;
+          wait_timed(bres_bar(kb), 0, p.timeout_ns);
+        }
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -213,7 +227,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      bool b_ready = !kResident;
+      bool first_tile = true;  // resident B: its k-blocks are still landing
       for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
         if (!wait_or_abort(tempty_bar(acc), acc_phase ^ 1u, p.timeout_ns, abort_flag,
                            kSiteTmemEmpty))
@@ -232,12 +246,10 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
           if (kResident) {
             const int kb = (k0 + i < p.num_k_blocks) ? k0 + i : k0 + i - p.num_k_blocks;
             b_src = base + L.bres + kb * p.katoms * p.b_atom_bytes;
-            if (!b_ready) {  // the resident B, once
-              if (!wait_or_abort(bres_bar, 0, p.timeout_ns, abort_flag, kSiteFull)) {
-                ok = false;
-                break;
-              }
-              b_ready = true;
+            if (first_tile &&
+                !wait_or_abort(bres_bar(kb), 0, p.timeout_ns, abort_flag, kSiteFull)) {
+              ok = false;
+              break;
             }
           }
           tc_fence_after_sync();
@@ -262,6 +274,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
         }
         if (!ok) break;
         umma_commit(tfull_bar(acc));      // accumulator complete
+        first_tile = false;
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1u;

@@ -73,9 +73,10 @@ uint32_t make_idesc(int m, int n) {
 
 // Deepest ring (at least 2) whose carve-up, plus 1 KiB of alignment slack,
 // fits the dynamic shared memory limit; 1 if not even 2 stages fit.
-int stages_that_fit(uint32_t stage_bytes, int epi_warps, uint32_t bres_bytes = 0) {
+int stages_that_fit(uint32_t stage_bytes, int epi_warps, uint32_t bres_bytes = 0,
+                    int bres_bars = 1) {
   const auto fits = [&](int s) {
-    return SmemLayout::make(s, stage_bytes, epi_warps, bres_bytes).total + 1024 <=
+    return SmemLayout::make(s, stage_bytes, epi_warps, bres_bytes, bres_bars).total + 1024 <=
            static_cast<uint32_t>(kMaxDynSmem);
   };
   if (!fits(2)) return 1;
@@ -297,10 +298,10 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
       if (b_resident || (o.epi_warps && ew != o.epi_warps)) continue;
       for (int ka : {2, 1}) {
         if (b_resident || (o.katoms && ka != o.katoms)) continue;
-        const uint32_t bres = static_cast<uint32_t>((K + kBK * ka - 1) / (kBK * ka)) * ka *
-                              b_atom_bytes_for(path, bn);
+        const int nk = static_cast<int>((K + kBK * ka - 1) / (kBK * ka));
+        const uint32_t bres = static_cast<uint32_t>(nk) * ka * b_atom_bytes_for(path, bn);
         if (bres > static_cast<uint32_t>(kMaxDynSmem)) continue;
-        const int f = stages_that_fit(static_cast<uint32_t>(ka) * kABytes, ew, bres);
+        const int f = stages_that_fit(static_cast<uint32_t>(ka) * kABytes, ew, bres, nk);
         if (f >= min_stages && (ka == 1 || o.katoms || f >= 3)) {
           b_resident = true;
           bres_bytes = bres;
@@ -349,11 +350,12 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
     if (stages > fit) return GEMM_ERR_INVALID_VALUE;
     smem_total = small_total(stages);
   } else {
-    const int fit = stages_that_fit(stage_bytes, epi_warps, bres_bytes);
+    const int bres_bars = b_resident ? static_cast<int>(num_k) : 1;  // one per k-block of B
+    const int fit = stages_that_fit(stage_bytes, epi_warps, bres_bytes, bres_bars);
     if (fit < 2) return GEMM_ERR_INVALID_VALUE;
     stages = o.kstage ? o.kstage : fit;
     if (stages > fit) return GEMM_ERR_INVALID_VALUE;
-    smem_total = SmemLayout::make(stages, stage_bytes, epi_warps, bres_bytes).total + 1024;
+    smem_total = SmemLayout::make(stages, stage_bytes, epi_warps, bres_bytes, bres_bars).total + 1024;
   }
   // Balanced grids: as many CTAs (pairs) as the fewest waves need, so every
   // one gets the same number of tiles (units) to one.  An HBM-bound stream

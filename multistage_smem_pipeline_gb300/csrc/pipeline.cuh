@@ -70,18 +70,19 @@ __device__ __forceinline__ int first_k_block(int t, const GemmParams& p) {
 
 // Shared-memory carve-up, offsets from the 1024-aligned base: the ring, the
 // resident B region (if any; 1024-aligned since stages are whole 16 KiB A
-// slices), the epilogue staging buffers, then 2 * stages + 6 mbarriers
-// (full, empty, 2 tmem-full, 2 tmem-empty, drain, resident-B full).
+// slices), the epilogue staging buffers, then 2 * stages + 5 + bres_bars
+// mbarriers (full, empty, 2 tmem-full, 2 tmem-empty, drain, then one per
+// k-block of the resident B -- one slot at least).
 struct SmemLayout {
   uint32_t ring, bres, epi, bars, misc, total;
   __host__ __device__ static SmemLayout make(int stages, uint32_t stage_bytes, int epi_warps,
-                                             uint32_t bres_bytes = 0) {
+                                             uint32_t bres_bytes = 0, int bres_bars = 1) {
     SmemLayout L;
     L.ring = 0;
     L.bres = stages * stage_bytes;
     L.epi = L.bres + bres_bytes;
     L.bars = L.epi + epi_warps * kEpiBufs * kEpiChunkBytes;
-    L.misc = L.bars + 8 * (2 * stages + 6);
+    L.misc = L.bars + 8 * (2 * stages + 5 + (bres_bars > 1 ? bres_bars : 1));
     L.total = L.misc + 16;
     return L;
   }

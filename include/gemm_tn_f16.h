@@ -36,7 +36,9 @@ typedef enum {
   GEMM_ERR_UNSUPPORTED_DEVICE = 3,/* current device is not compute capability 10.3 */
   GEMM_ERR_LAUNCH = 4,            /* the kernel launch itself failed */
   GEMM_ERR_TIMEOUT = 5,           /* a pipeline wait in the kernel gave up (see gemm_get_device_error) */
-  GEMM_ERR_CUDA = 6               /* another CUDA runtime error (no device, memset failed, ...) */
+  GEMM_ERR_CUDA = 6,              /* another CUDA runtime error (no device, memset failed, ...) */
+  GEMM_ERR_INVARIANT = 7          /* a pipeline invariant check failed (opt->check; see
+                                     gemm_get_device_error) */
 } gemm_status_t;
 
 /* Kernel paths. */
@@ -84,9 +86,12 @@ typedef struct {
                           waves of tiles (units), so each gets the same number to one */
   int group_m;         /* m-blocks per rasterisation group: 0 = choose           */
   uint64_t timeout_ns; /* per-wait limit inside the kernel: 0 = 2 s              */
-  int inject;          /* test hook: 1 = the producer announces its first stage
+  int inject;          /* test hooks: 1 = the producer announces its first stage
                           but never loads it, so the consumers' waits run out;
-                          the kernel then reports GEMM_ERR_TIMEOUT and exits   */
+                          the kernel then reports GEMM_ERR_TIMEOUT and exits.
+                          2 = the producer stamps its first ring slot with a
+                          wrong sequence number (nothing else changes), which
+                          `check` must report as GEMM_ERR_INVARIANT */
   int katoms;          /* 64-wide K slices per ring stage: 0 = choose, 1 or 2 (a
                           stage of 2 halves the per-byte barrier and commit work) */
   int epi_warps;       /* epilogue warps per CTA: 0 = choose, 4 or 8 (8 doubles the
@@ -118,6 +123,18 @@ typedef struct {
                           stages at bn = 96 where the single-CTA kernel fits three).
                           Otherwise the single-CTA kernel runs.  With the same
                           katoms the results are bit-identical. */
+  int check;           /* 1: verify the pipeline's invariants in the kernel (debug):
+                          the producer stamps every ring slot with the sequence
+                          number of the fill it issues there, and the MMA thread
+                          compares it, once the slot is full, with the count of
+                          slots it has consumed -- a wrong stage index or phase
+                          that still lets the pipeline run.  A mismatch records
+                          GEMM_ERR_INVARIANT (site 5) in the device error word;
+                          the kernel never traps and runs on.  Built for the plain
+                          forms (D stored by TMA, alpha = 1, beta = 0); with a
+                          scaled epilogue or a D stored directly (gemm_f16_padded
+                          with unaligned D rows) it is GEMM_ERR_INVALID_VALUE.
+                          0: off, at no cost: separate kernel instantiations */
   int split_k;         /* 0 = choose, 1 = never, 2 = always (else GEMM_ERR_INVALID_VALUE).
                           Split: a cluster of two CTAs computes each 128 x bn tile,
                           each CTA half of the k range; the two exchange their fp32
@@ -233,14 +250,16 @@ int gemm_query_config(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt
                       gemm_config_t* out);
 
 /* Synchronises `stream`, then returns and clears the device error word of the
- * current device: GEMM_OK, or GEMM_ERR_TIMEOUT if a kernel gave up waiting.
+ * current device: GEMM_OK, GEMM_ERR_TIMEOUT if a kernel gave up waiting, or
+ * GEMM_ERR_INVARIANT if a call with opt->check found a ring slot out of
+ * sequence (the first error of either kind is kept until read).
  * The word is one per device, shared by every stream and every call of this
  * library on the device: a timeout raised by a call on another stream is
  * reported (and cleared) by whichever poll reads the word first, and a poll
  * of `stream` does not wait for the other streams.
  * If `raw` is not NULL it receives the raw word (low byte = status, next byte
  * = the wait site that gave up: 1 producer/empty, 2 mma/full, 3 mma/tmem-empty,
- * 4 epilogue/tmem-full). */
+ * 4 epilogue/tmem-full; or 5, the invariant check of a ring slot). */
 int gemm_get_device_error(void* stream, uint32_t* raw);
 
 /* Minimum ring depth that hides a copy latency behind compute:

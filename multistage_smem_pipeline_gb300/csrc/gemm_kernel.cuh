@@ -46,6 +46,13 @@ __device__ __forceinline__ void record_error(uint32_t code, uint32_t site) {
   atomicCAS(&g_gemm_error, 0u, code | (site << 8));
 }
 
+// The MMA thread's half of the invariant check (see stamp_slot).
+template <bool kCheck>
+__device__ __forceinline__ void check_slot(const volatile uint32_t* seq, int stage,
+                                           uint32_t consumed) {
+  if (kCheck && seq[stage] != consumed) record_error(kErrInvariant, kSiteRingSeq);
+}
+
 // Wait for phase `parity` of `bar`; give up when the CTA is aborting or after
 // timeout_ns without completion (then record the error and start the abort).
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
@@ -68,8 +75,9 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uin
 // kResident selects the resident-B mode at compile time (p.b_resident must
 // agree), so the streaming kernel's loops carry none of its code.  kDirectD
 // stores D with plain stores to p.D (row stride p.ldd) instead of TMA stores
-// through tmD, which such kernels never touch.
-template <int kEpiWarps, bool kResident, bool kDirectD>
+// through tmD, which such kernels never touch.  kCheck adds the pipeline
+// invariant check (p.check), at no cost to the kernels without it.
+template <int kEpiWarps, bool kResident, bool kDirectD, bool kCheck = false>
 __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
     gemm_tn_f16_persistent(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
@@ -97,6 +105,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
   auto bres_bar = [&](int j) { return bars + 8u * (2 * S + 5 + j); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc + 4);
+  volatile uint32_t* const slot_seq = reinterpret_cast<volatile uint32_t*>(smem + L.misc + 8);
 
   if (threadIdx.x == 0) {
     // The next GEMM in the stream may start its own set-up on SMs this grid
@@ -176,6 +185,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
                           bres_bar(kb), (kb * p.katoms + at) * kBK, n_row);
             ++b_issued;
           }
+          stamp_slot<kCheck>(slot_seq, stage, issued, p);
           mbar_arrive_expect_tx(full_bar(stage), p.stage_bytes);
           if (!(p.inject == 1 && issued == 0)) {
             for (int at = 0; at < p.katoms; ++at) {
@@ -228,6 +238,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool first_tile = true;  // resident B: its k-blocks are still landing
+      uint32_t consumed = 0;   // ring slots consumed (the invariant check)
       for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
         if (!wait_or_abort(tempty_bar(acc), acc_phase ^ 1u, p.timeout_ns, abort_flag,
                            kSiteTmemEmpty))
@@ -241,6 +252,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
             ok = false;
             break;
           }
+          check_slot<kCheck>(slot_seq, stage, consumed++);
           const uint32_t a_src = base + L.ring + stage * p.stage_bytes;
           uint32_t b_src = a_src + p.katoms * kABytes;
           if (kResident) {

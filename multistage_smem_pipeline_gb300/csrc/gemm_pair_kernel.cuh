@@ -52,7 +52,8 @@ namespace gb300 {
 // accumulators are no longer double-buffered across units: the next unit's
 // MMAs wait until both are drained.  Each accumulator sees the same MMAs in
 // the same order as with kNT = 1, so the results are bit-identical.
-template <int kEpiWarps, bool kDirectD, int kNT, bool kScaled>
+// kCheck: the pipeline invariant check (as in gemm_tn_f16_persistent).
+template <int kEpiWarps, bool kDirectD, int kNT, bool kScaled, bool kCheck = false>
 __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
     gemm_tn_f16_pair(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB,
@@ -86,6 +87,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
   const uint32_t drain_bar = bars + 8u * (2 * S + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc + 4);
+  volatile uint32_t* const slot_seq = reinterpret_cast<volatile uint32_t*>(smem + L.misc + 8);
 
   if (threadIdx.x == 0) {
     grid_launch_dependents();  // see gemm_tn_f16_persistent
@@ -144,7 +146,10 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
           const uint32_t a_dst = base + L.ring + stage * p.stage_bytes;
           const uint32_t b_dst = a_dst + p.katoms * kABytes;
           const uint32_t leader_full = mapa_shared(full_bar(stage), 0);
-          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2u * p.stage_bytes);
+          if (rank == 0) {  // the even CTA's barrier counts both CTAs' bytes
+            stamp_slot<kCheck>(slot_seq, stage, issued, p);
+            mbar_arrive_expect_tx(full_bar(stage), 2u * p.stage_bytes);
+          }
           if (!(p.inject == 1 && issued == 0 && rank == 0)) {
             for (int at = 0; at < p.katoms; ++at) {
               const int x = (kb * p.katoms + at) * kBK;  // past K: the box reads zeros
@@ -190,6 +195,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
+      uint32_t consumed = 0;  // ring slots consumed (the invariant check)
       for (int t = pair; t < p.num_tiles; t += num_pairs) {
         bool drained = true;
         for (int j = 0; j < kNT && drained; ++j)
@@ -204,6 +210,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
             ok = false;
             break;
           }
+          check_slot<kCheck>(slot_seq, stage, consumed++);
           tc_fence_after_sync();
           const uint32_t a_src = base + L.ring + stage * p.stage_bytes;
           const uint32_t b_src = a_src + p.katoms * kABytes;

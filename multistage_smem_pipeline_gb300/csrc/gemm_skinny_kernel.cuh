@@ -53,14 +53,15 @@ struct SkinnyLayout {
     L.ring = 0;
     L.bars = stages * stage_bytes;
     L.misc = L.bars + 8 * (2 * stages + 2);
-    L.total = L.misc + 16;
+    L.total = L.misc + kMiscBytes;
     return L;
   }
 };
 // the epilogue's staging buffers fit in one ring stage
 static_assert(kSkinnyEpiWarps * kEpiBufs * kEpiChunkBytes <= kABytes, "staging exceeds a stage");
 
-template <bool kDirectD>
+// kCheck: the pipeline invariant check (as in gemm_tn_f16_persistent).
+template <bool kDirectD, bool kCheck = false>
 __global__ void __launch_bounds__(kSkinnyThreads, 1)
     gemm_tn_f16_skinny(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB,
@@ -82,6 +83,7 @@ __global__ void __launch_bounds__(kSkinnyThreads, 1)
   const uint32_t drain_bar = bars + 8u * (2 * S + 1);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc + 4);
+  volatile uint32_t* const slot_seq = reinterpret_cast<volatile uint32_t*>(smem + L.misc + 8);
 
   if (threadIdx.x == 0) {
     grid_launch_dependents();  // see gemm_tn_f16_persistent
@@ -129,6 +131,7 @@ __global__ void __launch_bounds__(kSkinnyThreads, 1)
           break;
         const uint32_t a_dst = base + L.ring + stage * p.stage_bytes;
         const uint32_t b_dst = a_dst + p.katoms * kABytes;
+        stamp_slot<kCheck>(slot_seq, stage, issued, p);
         mbar_arrive_expect_tx(full_bar(stage), p.stage_bytes);
         if (!(p.inject == 1 && issued == 0)) {
           for (int at = 0; at < p.katoms; ++at) {
@@ -167,6 +170,7 @@ __global__ void __launch_bounds__(kSkinnyThreads, 1)
           ok = false;
           break;
         }
+        check_slot<kCheck>(slot_seq, stage, static_cast<uint32_t>(i));
         tc_fence_after_sync();
         const uint32_t a_src = base + L.ring + stage * p.stage_bytes;
         const uint32_t b_src = a_src + p.katoms * kABytes;

@@ -52,7 +52,7 @@ struct SplitLayout {
     L.rx = stages * stage_bytes;
     L.bars = L.rx + static_cast<uint32_t>(bn) * 256u;
     L.misc = L.bars + 8 * (2 * stages + 3);
-    L.total = L.misc + 16;
+    L.total = L.misc + kMiscBytes;
     return L;
   }
 };
@@ -85,6 +85,8 @@ __device__ __forceinline__ uint32_t splitk_chunk_offset(int c, int q) {
   return static_cast<uint32_t>(c * 4 + q) * 4096u;
 }
 
+// kCheck: the pipeline invariant check (as in gemm_tn_f16_persistent).
+template <bool kCheck = false>
 __global__ void __launch_bounds__(kSplitThreads, 1)
     gemm_tn_f16_splitk(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB,
@@ -114,6 +116,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
   const uint32_t rx_full_bar = bars + 8u * (2 * S + 2);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc + 4);
+  volatile uint32_t* const slot_seq = reinterpret_cast<volatile uint32_t*>(smem + L.misc + 8);
 
   if (threadIdx.x == 0) {
     grid_launch_dependents();  // see gemm_tn_f16_persistent
@@ -161,6 +164,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
           break;
         const uint32_t a_dst = base + L.ring + stage * p.stage_bytes;
         const uint32_t b_dst = a_dst + p.katoms * kABytes;
+        stamp_slot<kCheck>(slot_seq, stage, issued, p);
         mbar_arrive_expect_tx(full_bar(stage), p.stage_bytes);
         if (!(p.inject == 1 && issued == 0)) {
           for (int at = 0; at < p.katoms; ++at) {
@@ -190,6 +194,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
           ok = false;
           break;
         }
+        check_slot<kCheck>(slot_seq, stage, static_cast<uint32_t>(i));
         tc_fence_after_sync();
         const uint32_t a_src = base + L.ring + stage * p.stage_bytes;
         const uint32_t b_src = a_src + p.katoms * kABytes;

@@ -123,9 +123,10 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   if (opt) o = *opt;
   if (o.path < 0 || o.path > 3 || o.bn < 0 || o.bn > 256 || (o.bn % 32) != 0 || o.kstage < 0 ||
       o.kstage == 1 || o.kstage > kMaxStages || o.max_ctas < 0 || o.group_m < 0 || o.inject < 0 ||
-      o.inject > 1 || o.katoms < 0 || o.katoms > 2 || o.acc_f16 < 0 || o.acc_f16 > 1 ||
+      o.inject > 2 || o.katoms < 0 || o.katoms > 2 || o.acc_f16 < 0 || o.acc_f16 > 1 ||
       o.b_resident < 0 || o.b_resident > 2 || o.pdl < 0 || o.pdl > 1 || o.wide < 0 ||
       o.wide > 2 || o.small_m < 0 || o.small_m > 2 || o.split_k < 0 || o.split_k > 2 ||
+      o.check < 0 || o.check > 1 ||
       (o.epi_warps != 0 && o.epi_warps != 4 && o.epi_warps != 8))
     return GEMM_ERR_INVALID_VALUE;
   if (o.path == GEMM_PATH_SKINNY && M > kBM) return GEMM_ERR_INVALID_VALUE;
@@ -437,6 +438,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   p.k_rotate = (num_m == 1 && num_n > 1) ? 1 : 0;
   p.timeout_ns = o.timeout_ns ? o.timeout_ns : kDefaultTimeoutNs;
   p.inject = o.inject;
+  p.check = o.check;
   *out = pl;
   return GEMM_OK;
 }
@@ -465,7 +467,7 @@ bool grant_smem(Kernel k) {
 // x scaled epilogue for the pair.
 template <bool kDirectD>
 bool grant_all(bool ok) {
-  return ok && grant_smem(gemm_tn_f16_skinny<kDirectD>) && grant_smem(gemm_tn_f16_splitk) &&
+  return ok && grant_smem(gemm_tn_f16_skinny<kDirectD>) && grant_smem(gemm_tn_f16_splitk<>) &&
          grant_smem(gemm_tn_f16_persistent<4, false, kDirectD>) &&
          grant_smem(gemm_tn_f16_persistent<8, false, kDirectD>) &&
          grant_smem(gemm_tn_f16_persistent<4, true, kDirectD>) &&
@@ -478,6 +480,43 @@ bool grant_all(bool ok) {
          grant_smem(gemm_tn_f16_pair<8, kDirectD, 1, true>) &&
          grant_smem(gemm_tn_f16_pair<4, kDirectD, 2, true>) &&
          grant_smem(gemm_tn_f16_pair<8, kDirectD, 2, true>);
+}
+
+// The invariant-checking instantiations: the plain forms (D stored by TMA,
+// no scaled epilogue) of every kernel.
+bool grant_checked() {
+  return grant_smem(gemm_tn_f16_skinny<false, true>) && grant_smem(gemm_tn_f16_splitk<true>) &&
+         grant_smem(gemm_tn_f16_persistent<4, false, false, true>) &&
+         grant_smem(gemm_tn_f16_persistent<8, false, false, true>) &&
+         grant_smem(gemm_tn_f16_persistent<4, true, false, true>) &&
+         grant_smem(gemm_tn_f16_persistent<8, true, false, true>) &&
+         grant_smem(gemm_tn_f16_pair<4, false, 1, false, true>) &&
+         grant_smem(gemm_tn_f16_pair<8, false, 1, false, true>) &&
+         grant_smem(gemm_tn_f16_pair<4, false, 2, false, true>) &&
+         grant_smem(gemm_tn_f16_pair<8, false, 2, false, true>);
+}
+
+cudaError_t launch_checked(const cudaLaunchConfig_t& cfg, bool pair, bool wide, bool resident,
+                           bool small, bool split, int epi_warps, const CUtensorMap& a,
+                           const CUtensorMap& b, const CUtensorMap& d, const GemmParams& p) {
+  if (split) return cudaLaunchKernelEx(&cfg, gemm_tn_f16_splitk<true>, a, b, d, p);
+  if (small) return cudaLaunchKernelEx(&cfg, gemm_tn_f16_skinny<false, true>, a, b, d, p);
+  if (pair) {
+    if (wide)
+      return epi_warps == 8
+                 ? cudaLaunchKernelEx(&cfg, gemm_tn_f16_pair<8, false, 2, false, true>, a, b, d, p)
+                 : cudaLaunchKernelEx(&cfg, gemm_tn_f16_pair<4, false, 2, false, true>, a, b, d, p);
+    return epi_warps == 8
+               ? cudaLaunchKernelEx(&cfg, gemm_tn_f16_pair<8, false, 1, false, true>, a, b, d, p)
+               : cudaLaunchKernelEx(&cfg, gemm_tn_f16_pair<4, false, 1, false, true>, a, b, d, p);
+  }
+  if (resident)
+    return epi_warps == 8
+               ? cudaLaunchKernelEx(&cfg, gemm_tn_f16_persistent<8, true, false, true>, a, b, d, p)
+               : cudaLaunchKernelEx(&cfg, gemm_tn_f16_persistent<4, true, false, true>, a, b, d, p);
+  return epi_warps == 8
+             ? cudaLaunchKernelEx(&cfg, gemm_tn_f16_persistent<8, false, false, true>, a, b, d, p)
+             : cudaLaunchKernelEx(&cfg, gemm_tn_f16_persistent<4, false, false, true>, a, b, d, p);
 }
 
 template <bool kDirectD, int kNT, bool kScaled>
@@ -518,7 +557,7 @@ int prepare_device(DeviceState* st) {
   std::lock_guard<std::mutex> lk(g_mu);
   if (st->smem_attr == kMaxDynSmem && st->pair_smem_attr == kMaxDynSmem && st->max_pairs > 0)
     return GEMM_OK;
-  if (!grant_all<true>(grant_all<false>(true))) {
+  if (!grant_all<true>(grant_all<false>(true)) || !grant_checked()) {
     cudaGetLastError();
     return GEMM_ERR_CUDA;
   }
@@ -692,8 +731,12 @@ int launch_gemm(int64_t M, int64_t N, int64_t K, const View& a, const View& b, c
   cfg.attrs = attr;
   cfg.numAttrs = nattr;
   const bool wide = pl.cfg.wide != 0, res = pl.p.b_resident != 0, small = pl.cfg.small_m != 0;
+  // the invariant check exists for the plain forms only: D stored by TMA, no scaled epilogue
+  if (pl.p.check && (d_direct || pl.p.scaled)) return GEMM_ERR_INVALID_VALUE;
   const cudaError_t e =
-      pl.cfg.split_k ? cudaLaunchKernelEx(&cfg, gemm_tn_f16_splitk, tmA, tmB, tmD, pl.p) :
+      pl.p.check ? launch_checked(cfg, pair, wide, res, small, pl.cfg.split_k != 0,
+                                  pl.cfg.epi_warps, tmA, tmB, tmD, pl.p) :
+      pl.cfg.split_k ? cudaLaunchKernelEx(&cfg, gemm_tn_f16_splitk<>, tmA, tmB, tmD, pl.p) :
       d_direct ? launch_kernel<true>(cfg, pair, wide, res, small, pl.cfg.epi_warps, tmA, tmB, tmD,
                                      pl.p)
                : launch_kernel<false>(cfg, pair, wide, res, small, pl.cfg.epi_warps, tmA, tmB,
@@ -814,6 +857,7 @@ extern "C" const char* gemm_status_string(int status) {
     case GEMM_ERR_LAUNCH: return "GEMM_ERR_LAUNCH";
     case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT";
     case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA";
+    case GEMM_ERR_INVARIANT: return "GEMM_ERR_INVARIANT";
     default: return "GEMM_ERR_UNKNOWN";
   }
 }

@@ -22,9 +22,17 @@ constexpr int kEpiCols = 32;         // columns per epilogue chunk (one tcgen05.
 constexpr uint32_t kEpiChunkBytes = 32 * kEpiCols * 2;  // 32 rows x 32 fp16
 constexpr uint32_t kABytes = kBM * kBK * 2;             // 16 KiB
 constexpr int kMaxStages = 16;
-constexpr uint32_t kErrTimeout = 5;  // == GEMM_ERR_TIMEOUT
+constexpr uint32_t kErrTimeout = 5;    // == GEMM_ERR_TIMEOUT
+constexpr uint32_t kErrInvariant = 7;  // == GEMM_ERR_INVARIANT
 
 enum WaitSite : uint32_t { kSiteEmpty = 1, kSiteFull = 2, kSiteTmemEmpty = 3, kSiteTmemFull = 4 };
+// Site of a failed invariant check: the ring slot the MMA thread consumed did
+// not carry the sequence number of the fill it expected.
+constexpr uint32_t kSiteRingSeq = 5;
+
+// Bytes after the misc area's TMEM slot and abort flag (8 bytes): one
+// sequence word per ring slot for the invariant check, kMaxStages of them.
+constexpr uint32_t kMiscBytes = 8 + 4 * 16;
 
 struct GemmParams {
   int32_t M, N, K;
@@ -53,6 +61,7 @@ struct GemmParams {
   uint32_t bres_bytes;   // size of that region: num_k_blocks * katoms * b_atom_bytes (else 0)
   uint16_t* D;           // direct-store kernels only: D (rows not 16-byte aligned) ...
   int64_t ldd;           // ... and its row stride in elements
+  int32_t check;         // 1: the MMA thread checks each ring slot's fill sequence number
 };
 
 // MN-major B: one 64-element N chunk per TMA box; chunks 8 KiB apart.
@@ -83,7 +92,7 @@ struct SmemLayout {
     L.epi = L.bres + bres_bytes;
     L.bars = L.epi + epi_warps * kEpiBufs * kEpiChunkBytes;
     L.misc = L.bars + 8 * (2 * stages + 5 + (bres_bars > 1 ? bres_bars : 1));
-    L.total = L.misc + 16;
+    L.total = L.misc + kMiscBytes;
     return L;
   }
 };
@@ -116,6 +125,21 @@ __device__ __forceinline__ void tile_coords(int t, const GemmParams& p, int& mb,
   const int in = t - g * group_tiles;
   mb = first_m + in % gm;
   nb = in / gm;
+}
+
+// The pipeline invariant check (the kernels' kCheck instantiations, chosen
+// for p.check): the producer stamps ring slot s
+// with the sequence number of the fill it issues there (written before its
+// arrive on the slot's full barrier, which orders it), and the MMA thread,
+// once the slot is full, compares the stamp with the count of slots it has
+// consumed.  A wrong stage index or phase that still lets the pipeline run
+// shows up as a mismatch, recorded as GEMM_ERR_INVARIANT | site << 8 in the
+// device error word; the kernel goes on (no trap).  inject == 2 plants one
+// wrong stamp, to test the check.
+template <bool kCheck>
+__device__ __forceinline__ void stamp_slot(volatile uint32_t* seq, int stage, uint32_t issued,
+                                           const GemmParams& p) {
+  if (kCheck) seq[stage] = issued + ((p.inject == 2 && issued == 0) ? 1u : 0u);
 }
 
 __device__ __forceinline__ uint32_t pack_half2(uint32_t lo_bits, uint32_t hi_bits) {

@@ -99,12 +99,13 @@ def test_empty_output_is_a_noop_without_device(binding):
 
 def test_rejects_bad_options(binding):
     for kw in [dict(bn=48), dict(bn=512), dict(kstage=1), dict(kstage=17), dict(path=4),
-               dict(inject=2), dict(max_ctas=-1), dict(path=binding.PATH_SKINNY),
+               dict(inject=3), dict(max_ctas=-1), dict(path=binding.PATH_SKINNY),
                dict(katoms=3), dict(katoms=-1), dict(epi_warps=6), dict(epi_warps=16),
                dict(acc_f16=2), dict(b_resident=3), dict(b_resident=-1),
                dict(b_resident=2, path=binding.PATH_PAIR),
                dict(b_resident=2, bn=32, group_m=4), dict(wide=3), dict(wide=-1),
-               dict(wide=2, path=binding.PATH_SQUARE)]:
+               dict(wide=2, path=binding.PATH_SQUARE), dict(check=2), dict(check=-1),
+               dict(split_k=3), dict(small_m=3)]:
         o = binding._options(**kw)
         M = 256 if kw.get("path") == binding.PATH_SKINNY else 64
         assert _call(binding, P0, P1, P2, M, 64, 64, o) == binding.GEMM_ERR_INVALID_VALUE, kw
@@ -179,6 +180,7 @@ def test_scaled_entry_rejects_bad_arguments(binding):
 def test_status_strings(binding):
     assert binding.status_string(0) == "GEMM_OK"
     assert binding.status_string(5) == "GEMM_ERR_TIMEOUT"
+    assert binding.status_string(7) == "GEMM_ERR_INVARIANT"
     assert binding.status_string(99) == "GEMM_ERR_UNKNOWN"
 
 

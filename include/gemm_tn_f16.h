@@ -249,14 +249,15 @@ typedef struct {
 int gemm_query_config(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt,
                       gemm_config_t* out);
 
-/* Synchronises `stream`, then returns and clears the device error word of the
- * current device: GEMM_OK, GEMM_ERR_TIMEOUT if a kernel gave up waiting, or
- * GEMM_ERR_INVARIANT if a call with opt->check found a ring slot out of
- * sequence (the first error of either kind is kept until read).
- * The word is one per device, shared by every stream and every call of this
- * library on the device: a timeout raised by a call on another stream is
- * reported (and cleared) by whichever poll reads the word first, and a poll
- * of `stream` does not wait for the other streams.
+/* Synchronises `stream`, then returns and clears the device error word of
+ * `stream` on the current device: GEMM_OK, GEMM_ERR_TIMEOUT if a kernel
+ * launched on it gave up waiting, or GEMM_ERR_INVARIANT if a call with
+ * opt->check found a ring slot out of sequence (the first error is kept until
+ * read).  Each stream has its own word: the legacy default stream (NULL) and
+ * the first 63 other streams a process passes to this library; streams beyond
+ * those share words by a hash of their handle, so a poll may then also report
+ * (and clear) another stream's error.  A kernel captured in a CUDA graph
+ * reports to the word of the stream it was captured on.
  * If `raw` is not NULL it receives the raw word (low byte = status, next byte
  * = the wait site that gave up: 1 producer/empty, 2 mma/full, 3 mma/tmem-empty,
  * 4 epilogue/tmem-full; or 5, the invariant check of a ring slot). */

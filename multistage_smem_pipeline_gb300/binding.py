@@ -268,7 +268,7 @@ def gemm_tn_f16_from_host(a_host: torch.Tensor, b_host: torch.Tensor, device=Non
 
 
 def get_device_error(stream=None) -> tuple[int, int]:
-    """(status, raw word) of the device error word; synchronises the stream and clears it."""
+    """(status, raw word) of the stream's device error word; synchronises the stream and clears it."""
     raw = ctypes.c_uint32(0)
     rc = LIB.gemm_get_device_error(_stream_handle(stream), ctypes.byref(raw))
     return rc, int(raw.value)

@@ -40,17 +40,27 @@
 
 namespace gb300 {
 
-__device__ unsigned int g_gemm_error;  // first error of any kernel on this device (0 = none)
+// The device error words: the first error of the kernels launched on a given
+// stream (the host maps streams to words), 0 = none.
+__device__ unsigned int g_gemm_error[kErrorSlots];
 
-__device__ __forceinline__ void record_error(uint32_t code, uint32_t site) {
-  atomicCAS(&g_gemm_error, 0u, code | (site << 8));
+// `state` is the CTA's abort flag, followed by the index of its error word.
+__device__ __forceinline__ void record_error(uint32_t code, uint32_t site,
+                                             const volatile int* state) {
+  atomicCAS(&g_gemm_error[static_cast<uint32_t>(state[1]) % kErrorSlots], 0u, code | (site << 8));
+}
+
+// The CTA's abort flag and error-word index, set by one thread at start-up.
+__device__ __forceinline__ void init_abort_state(volatile int* state, const GemmParams& p) {
+  state[0] = 0;
+  state[1] = p.err_slot;
 }
 
 // The MMA thread's half of the invariant check (see stamp_slot).
 template <bool kCheck>
 __device__ __forceinline__ void check_slot(const volatile uint32_t* seq, int stage,
-                                           uint32_t consumed) {
-  if (kCheck && seq[stage] != consumed) record_error(kErrInvariant, kSiteRingSeq);
+                                           uint32_t consumed, const volatile int* state) {
+  if (kCheck && seq[stage] != consumed) record_error(kErrInvariant, kSiteRingSeq, state);
 }
 
 // Wait for phase `parity` of `bar`; give up when the CTA is aborting or after
@@ -65,7 +75,7 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uin
       if (*abort_flag) return false;
       if (global_timer_ns() - t0 > timeout_ns) {
         *abort_flag = 1;
-        record_error(kErrTimeout, site);
+        record_error(kErrTimeout, site, abort_flag);
         return false;
       }
     }
@@ -105,7 +115,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
   auto bres_bar = [&](int j) { return bars + 8u * (2 * S + 5 + j); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc + 4);
-  volatile uint32_t* const slot_seq = reinterpret_cast<volatile uint32_t*>(smem + L.misc + 8);
+  volatile uint32_t* const slot_seq = reinterpret_cast<volatile uint32_t*>(smem + L.misc + kMiscSlotSeq);
 
   if (threadIdx.x == 0) {
     // The next GEMM in the stream may start its own set-up on SMs this grid
@@ -123,7 +133,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
     if (kResident)
       for (int j = 0; j < p.num_k_blocks; ++j)
         mbar_init(bres_bar(j), 1);  // producer's arrive.expect_tx for k-block j of B
-    *abort_flag = 0;
+    init_abort_state(abort_flag, p);
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -252,7 +262,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
             ok = false;
             break;
           }
-          check_slot<kCheck>(slot_seq, stage, consumed++);
+          check_slot<kCheck>(slot_seq, stage, consumed++, abort_flag);
           const uint32_t a_src = base + L.ring + stage * p.stage_bytes;
           uint32_t b_src = a_src + p.katoms * kABytes;
           if (kResident) {

@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
   const uint32_t drain_bar = bars + 8u * (2 * S + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc + 4);
-  volatile uint32_t* const slot_seq = reinterpret_cast<volatile uint32_t*>(smem + L.misc + 8);
+  volatile uint32_t* const slot_seq = reinterpret_cast<volatile uint32_t*>(smem + L.misc + kMiscSlotSeq);
 
   if (threadIdx.x == 0) {
     grid_launch_dependents();  // see gemm_tn_f16_persistent
@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
       mbar_init(tempty_bar(b), 2 * kEpiWarps);  // every epilogue warp of both CTAs
     }
     mbar_init(drain_bar, 1);
-    *abort_flag = 0;
+    init_abort_state(abort_flag, p);
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
             ok = false;
             break;
           }
-          check_slot<kCheck>(slot_seq, stage, consumed++);
+          check_slot<kCheck>(slot_seq, stage, consumed++, abort_flag);
           tc_fence_after_sync();
           const uint32_t a_src = base + L.ring + stage * p.stage_bytes;
           const uint32_t b_src = a_src + p.katoms * kABytes;

@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(kSkinnyThreads, 1)
   const uint32_t drain_bar = bars + 8u * (2 * S + 1);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc + 4);
-  volatile uint32_t* const slot_seq = reinterpret_cast<volatile uint32_t*>(smem + L.misc + 8);
+  volatile uint32_t* const slot_seq = reinterpret_cast<volatile uint32_t*>(smem + L.misc + kMiscSlotSeq);
 
   if (threadIdx.x == 0) {
     grid_launch_dependents();  // see gemm_tn_f16_persistent
@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(kSkinnyThreads, 1)
     }
     mbar_init(tfull_bar, 1);       // tcgen05.commit after the tile's last k-block
     mbar_init(drain_bar, 1);
-    *abort_flag = 0;
+    init_abort_state(abort_flag, p);
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(kSkinnyThreads, 1)
           ok = false;
           break;
         }
-        check_slot<kCheck>(slot_seq, stage, static_cast<uint32_t>(i));
+        check_slot<kCheck>(slot_seq, stage, static_cast<uint32_t>(i), abort_flag);
         tc_fence_after_sync();
         const uint32_t a_src = base + L.ring + stage * p.stage_bytes;
         const uint32_t b_src = a_src + p.katoms * kABytes;

@@ -69,7 +69,7 @@ __device__ __forceinline__ bool wait_cluster_or_abort(uint32_t bar, uint32_t par
       if (*abort_flag) return false;
       if (global_timer_ns() - t0 > timeout_ns) {
         *abort_flag = 1;
-        record_error(kErrTimeout, site);
+        record_error(kErrTimeout, site, abort_flag);
         return false;
       }
     }
@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
   const uint32_t rx_full_bar = bars + 8u * (2 * S + 2);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc + 4);
-  volatile uint32_t* const slot_seq = reinterpret_cast<volatile uint32_t*>(smem + L.misc + 8);
+  volatile uint32_t* const slot_seq = reinterpret_cast<volatile uint32_t*>(smem + L.misc + kMiscSlotSeq);
 
   if (threadIdx.x == 0) {
     grid_launch_dependents();  // see gemm_tn_f16_persistent
@@ -129,7 +129,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     mbar_init(rx_full_bar, 1);
     // the peer's bulk copies of this CTA's half complete these bytes
     mbar_arrive_expect_tx(rx_full_bar, static_cast<uint32_t>(p.bn) * 256u);
-    *abort_flag = 0;
+    init_abort_state(abort_flag, p);
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
           ok = false;
           break;
         }
-        check_slot<kCheck>(slot_seq, stage, static_cast<uint32_t>(i));
+        check_slot<kCheck>(slot_seq, stage, static_cast<uint32_t>(i), abort_flag);
         tc_fence_after_sync();
         const uint32_t a_src = base + L.ring + stage * p.stage_bytes;
         const uint32_t b_src = a_src + p.katoms * kABytes;

@@ -586,6 +586,26 @@ int prepare_device(DeviceState* st) {
   return GEMM_OK;
 }
 
+// Device error words are per stream: the legacy default stream has word 0,
+// the first 63 other streams a process uses get one each, and later streams
+// share the remaining words by a hash of their handle.
+std::mutex g_slot_mu;
+uintptr_t g_slot_stream[kErrorSlots];
+int g_slots_used = 1;
+
+int error_slot(cudaStream_t s) {
+  const uintptr_t h = reinterpret_cast<uintptr_t>(s);
+  if (h == 0) return 0;
+  std::lock_guard<std::mutex> lk(g_slot_mu);
+  for (int i = 1; i < g_slots_used; ++i)
+    if (g_slot_stream[i] == h) return i;
+  if (g_slots_used < kErrorSlots) {
+    g_slot_stream[g_slots_used] = h;
+    return g_slots_used++;
+  }
+  return 1 + static_cast<int>((h >> 4) % static_cast<uintptr_t>(kErrorSlots - 1));
+}
+
 int check_args(const void* D, const void* A, const void* B, int64_t M, int64_t N, int64_t K) {
   if (M < 0 || N < 0 || K < 0 || M > INT_MAX || N > INT_MAX || K > INT_MAX)
     return GEMM_ERR_INVALID_VALUE;
@@ -683,6 +703,7 @@ int launch_gemm(int64_t M, int64_t N, int64_t K, const View& a, const View& b, c
   if (rc != GEMM_OK) return rc;
   if ((rc = get_encoder()) != GEMM_OK) return rc;
   pl.p.ldc = ldc;
+  pl.p.err_slot = error_slot(stream);
   if (sc && !(sc->alpha == 1.0f && sc->beta == 0.0f)) {
     pl.p.scaled = 1;
     pl.p.alpha = sc->alpha;
@@ -830,10 +851,11 @@ extern "C" int gemm_get_device_error(void* stream, uint32_t* raw) {
   unsigned int word = 0;
   const unsigned int zero = 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t off = static_cast<size_t>(error_slot(s)) * sizeof(unsigned int);
   if (cudaStreamSynchronize(s) != cudaSuccess ||
-      cudaMemcpyFromSymbolAsync(&word, g_gemm_error, sizeof(word), 0, cudaMemcpyDeviceToHost, s) !=
-          cudaSuccess ||
-      cudaMemcpyToSymbolAsync(g_gemm_error, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, s) !=
+      cudaMemcpyFromSymbolAsync(&word, g_gemm_error, sizeof(word), off, cudaMemcpyDeviceToHost,
+                                s) != cudaSuccess ||
+      cudaMemcpyToSymbolAsync(g_gemm_error, &zero, sizeof(zero), off, cudaMemcpyHostToDevice, s) !=
           cudaSuccess ||
       cudaStreamSynchronize(s) != cudaSuccess) {
     cudaGetLastError();

@@ -30,9 +30,15 @@ enum WaitSite : uint32_t { kSiteEmpty = 1, kSiteFull = 2, kSiteTmemEmpty = 3, kS
 // not carry the sequence number of the fill it expected.
 constexpr uint32_t kSiteRingSeq = 5;
 
-// Bytes after the misc area's TMEM slot and abort flag (8 bytes): one
-// sequence word per ring slot for the invariant check, kMaxStages of them.
-constexpr uint32_t kMiscBytes = 8 + 4 * 16;
+// The misc area: the TMEM base address (+0), the CTA's abort flag (+4), the
+// index of the error word its errors go to (+8), then from +16 one sequence
+// word per ring slot for the invariant check, kMaxStages of them.
+constexpr uint32_t kMiscBytes = 16 + 4 * 16;
+constexpr uint32_t kMiscSlotSeq = 16;
+
+// Error words per device: the host gives each stream its own (see
+// error_slot), the kernels record their first error there.
+constexpr int kErrorSlots = 64;
 
 struct GemmParams {
   int32_t M, N, K;
@@ -62,6 +68,7 @@ struct GemmParams {
   uint16_t* D;           // direct-store kernels only: D (rows not 16-byte aligned) ...
   int64_t ldd;           // ... and its row stride in elements
   int32_t check;         // 1: the MMA thread checks each ring slot's fill sequence number
+  int32_t err_slot;      // index of the device error word this call's errors go to
 };
 
 // MN-major B: one 64-element N chunk per TMA box; chunks 8 KiB apart.

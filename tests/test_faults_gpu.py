@@ -42,6 +42,31 @@ def test_stalled_stage_times_out_and_context_survives(lib, gpu, path):
     assert lib.get_device_error()[0] == lib.GEMM_OK
 
 
+def test_error_words_are_per_stream(lib, gpu):
+    """A timeout raised on one stream is reported by that stream's poll only."""
+    a_bits = synthetic.uniform_pm1(3, (256, 512))
+    b_bits = synthetic.uniform_pm1(4, (512, 512))
+    a = torch.from_numpy(a_bits.view(np.float16)).to(gpu)
+    b = torch.from_numpy(b_bits.view(np.float16)).to(gpu)
+    sx, sy = torch.cuda.Stream(gpu), torch.cuda.Stream(gpu)
+    for s in (sx, sy):
+        s.wait_stream(torch.cuda.current_stream(gpu))
+        assert lib.get_device_error(stream=s)[0] == lib.GEMM_OK
+    assert lib.get_device_error()[0] == lib.GEMM_OK
+    with torch.cuda.stream(sx):
+        lib.gemm_tn_f16_ex(a, b, inject=1, timeout_ns=50_000_000, max_ctas=2, stream=sx)
+    with torch.cuda.stream(sy):
+        d = lib.gemm_tn_f16_ex(a, b, stream=sy)
+    sx.synchronize()
+    assert lib.get_device_error(stream=sy)[0] == lib.GEMM_OK      # Y's word is clean
+    assert lib.get_device_error()[0] == lib.GEMM_OK               # so is the default stream's
+    assert lib.get_device_error(stream=sx)[0] == lib.GEMM_ERR_TIMEOUT
+    assert lib.get_device_error(stream=sx)[0] == lib.GEMM_OK      # reading clears it
+    st = compare(d.cpu().numpy().view(np.uint16), oracle.gemm_tn(a_bits, b_bits), 512,
+                 a_bits, b_bits)
+    assert st["bad"] == 0
+
+
 def test_latency_probes_give_a_stage_count(lib, gpu):
     copy, compute = lib.probe_latencies(bn=256, ctas=0, footprint_bytes=1 << 30, reps=32)
     assert copy > 0 and compute > 0

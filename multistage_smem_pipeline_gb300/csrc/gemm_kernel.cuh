@@ -140,6 +140,27 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     if (!kDirectD) tma_prefetch_desc(&tmD);
+    // The first ring of this CTA's first tile, fetched into L2 while the
+    // previous grid finishes (see tma_prefetch_l2_2d).
+    const int t0 = static_cast<int>(blockIdx.x);
+    if (t0 < p.num_tiles) {
+      int mb, nb;
+      tile_coords(t0, p, mb, nb);
+      const int kf = first_k_block(t0, p);
+      for (int i = 0; i < p.num_k_blocks && i < S; ++i) {
+        const int kb = (kf + i < p.num_k_blocks) ? kf + i : kf + i - p.num_k_blocks;
+        for (int at = 0; at < p.katoms; ++at) {
+          const int x = (kb * p.katoms + at) * kBK;
+          tma_prefetch_l2_2d(&tmA, x, mb * kBM);
+          if (p.b_kn) {
+            for (int ch = 0; ch < p.bn / 64; ++ch) tma_prefetch_l2_2d(&tmB, nb * p.bn + 64 * ch, x);
+          } else {
+            tma_prefetch_l2_2d(&tmB, x, kResident ? static_cast<int>(blockIdx.x % p.num_n_blocks) * p.bn
+                                                  : nb * p.bn);
+          }
+        }
+      }
+    }
   }
   __syncwarp();  // reconverge warp 0 before the aligned CTA barrier
   __syncthreads();  // barriers initialised: the producer may start loading at once

@@ -100,6 +100,21 @@ __global__ void __launch_bounds__(kSkinnyThreads, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     if (!kDirectD) tma_prefetch_desc(&tmD);
+    // The first ring of this CTA's operand boxes, fetched into L2 while the
+    // previous grid finishes (see tma_prefetch_l2_2d).
+    const int kf = first_k_block(t, p);
+    for (int i = 0; i < p.num_k_blocks && i < S; ++i) {
+      const int kb = (kf + i < p.num_k_blocks) ? kf + i : kf + i - p.num_k_blocks;
+      for (int at = 0; at < p.katoms; ++at) {
+        const int x = (kb * p.katoms + at) * kBK;
+        tma_prefetch_l2_2d(&tmA, x, 0);
+        if (p.b_kn) {
+          for (int ch = 0; ch < p.bn / 64; ++ch) tma_prefetch_l2_2d(&tmB, t * p.bn + 64 * ch, x);
+        } else {
+          tma_prefetch_l2_2d(&tmB, x, t * p.bn);
+        }
+      }
+    }
   }
   __syncwarp();
   __syncthreads();  // barriers initialised: the producer may start at once

@@ -8,7 +8,7 @@
 // guarded by full and empty barriers, here TMA loads and tcgen05.mma).  Then
 // each CTA finalises half of the tile's columns: CTA r keeps columns
 // [r BN/2, (r+1) BN/2), sends its fp32 partial of the other half into the
-// peer's shared memory (st.shared::cluster), receives the peer's partial of
+// peer's shared memory (st.async), receives the peer's partial of
 // its own half, adds the two, rounds to fp16 and stores D.  Per CTA that is
 // half the k-blocks of a 128 x BN tile -- at 1024^3 with BN = 128, 256 KiB of
 // operands and 32 MMAs per CTA instead of 384 KiB and 64 for a 128 x 64 tile
@@ -16,16 +16,17 @@
 //
 // The peer's partial lands in a region of its own after the ring
 // (128 x BN/2 x 4 bytes), so a CTA may send as soon as its own MMAs are done,
-// without waiting for the peer's.  Each epilogue warp writes its 32 x 32
-// chunk of the peer's half into its own ring (idle once the CTA's MMAs have
-// completed: one tile per pair) and one lane moves it with a bulk copy into
-// the peer's region, whose bytes complete on the peer's receive barrier (one
-// expect_tx of the whole half, made at set-up).  The epilogue's staging
-// buffers for D also reuse the ring.  Eight epilogue warps, two per TMEM lane
+// without waiting for the peer's.  Each epilogue warp loads its 32 x 32
+// chunk of the peer's half from TMEM and stores it from registers into the
+// peer's region with 16-byte remote stores whose bytes complete on the peer's
+// receive barrier (one expect_tx of the whole half, made at set-up).  The
+// epilogue's staging buffers for D reuse the ring, idle once the CTA's MMAs
+// have completed (one tile per pair).  Eight epilogue warps, two per TMEM lane
 // quadrant, each send and finish every other 32-column chunk.  The final
 // value of an element is p0 + p1 in fp32 whichever CTA forms it, so the
 // result does not depend on the pair's timing.  Every wait is bounded; both
-// CTAs meet on a cluster barrier before either exits.
+// CTAs meet on a cluster barrier before either exits (a relaxed one: each has
+// already seen the peer's partial land, so it need not wait for its stores).
 #pragma once
 #include "gemm_kernel.cuh"
 
@@ -35,10 +36,9 @@ constexpr int kSplitEpiWarps = 8;
 constexpr int kSplitThreads = 64 + 32 * kSplitEpiWarps;  // producer, MMA, epilogue
 constexpr uint32_t kSplitStagingBytes = kSplitEpiWarps * kEpiBufs * kEpiChunkBytes;  // 32 KiB
 
-// Bytes of ring the epilogue reuses: the staging buffers for D, then this
-// CTA's partial of the peer's half on its way out.
-__host__ __device__ constexpr uint32_t splitk_ring_reuse_bytes(int bn) {
-  return kSplitStagingBytes + static_cast<uint32_t>(bn) * 256u;
+// Bytes of ring the epilogue reuses: the staging buffers for D.
+__host__ __device__ constexpr uint32_t splitk_ring_reuse_bytes(int /*bn*/) {
+  return kSplitStagingBytes;
 }
 
 // Shared-memory carve-up, offsets from the 1024-aligned base: the ring (see
@@ -231,28 +231,25 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     if (ok) {
       tc_fence_after_sync();
       fence_proxy_async_smem();  // the ring's last async-proxy uses precede the writes below
-      // 1. send this CTA's partial of the peer's half: through this CTA's idle
-      // ring, one bulk copy per warp and chunk into the peer's region
-      const uint32_t out = base + L.ring + kSplitStagingBytes;
+      // 1. send this CTA's partial of the peer's half straight from registers
+      // into the peer's region: 16-byte remote stores whose bytes complete on
+      // the peer's receive barrier
+      const uint32_t rx_peer = mapa_shared(rx, peer) + lane * 16u;
+      const uint32_t rx_full_peer = mapa_shared(rx_full_bar, peer);
       for (int c = sel; c < half / kEpiCols; c += 2) {
         const uint32_t off = splitk_chunk_offset(c, q);
+        uint32_t r[32];
         if (rows_live) {
-          uint32_t r[32];
           tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(peer * half + c * kEpiCols), r);
           tmem_ld_wait();
+        } else {  // rows past M: the peer stores nothing there, but the bytes are counted
 #pragma unroll
-          for (int g = 0; g < 8; ++g)
-            st_shared_v4(out + off + g * 512u + lane * 16u, r[4 * g], r[4 * g + 1], r[4 * g + 2],
-                         r[4 * g + 3]);
+          for (int i = 0; i < 32; ++i) r[i] = 0u;
         }
-        // rows past M send whatever the ring holds: the peer stores nothing there
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          bulk_copy_to_cluster(mapa_shared(rx + off, peer), out + off, 4096u,
-                               mapa_shared(rx_full_bar, peer));
-          bulk_commit_group();
-        }
+#pragma unroll
+        for (int g = 0; g < 8; ++g)
+          st_async_cluster_v4(rx_peer + off + g * 512u, r[4 * g], r[4 * g + 1], r[4 * g + 2],
+                              r[4 * g + 3], rx_full_peer);
       }
       // 2. the peer's partial of this CTA's half: add, round, store (the warp
       // goes on only if every lane saw it land, so the tcgen05.ld below stays
@@ -312,7 +309,10 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
 
   __syncwarp();
   tc_fence_before_sync();
-  cluster_sync();  // no copy or arrive targets a CTA that has left
+  // Each CTA has seen the peer's copy land (rx-full) before it gets here, so
+  // no copy targets a CTA that has left; the arrive need not wait for the D
+  // stores.
+  cluster_sync_relaxed();
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc(tmem_base, p.tmem_cols);

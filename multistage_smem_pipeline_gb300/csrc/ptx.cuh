@@ -77,6 +77,17 @@ __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
+// Asks L2 to fetch one box of a 2-D tensor: no shared memory is written and
+// there is no completion to wait for.  It is only a hint: L2 is the device's
+// point of coherence, so a line fetched before another grid writes it is
+// updated by that write, and a later load still sees the new data.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 // Programmatic dependent launch.  launch_dependents lets the next kernel in
 // the stream (if it was launched with programmatic serialization) be
 // scheduled before this one ends; wait blocks until every prerequisite grid
@@ -278,6 +289,16 @@ __device__ __forceinline__ void cluster_sync() {
                    : "memory");
 }
 
+// The same meeting point without the release: the arrive does not wait for
+// this thread's earlier writes (the D stores still in flight) to be performed.
+// Only for the end of a kernel whose CTAs have already waited for every
+// remote write into their shared memory, where the barrier just keeps each
+// CTA's shared memory alive until its peer is past its own last access.
+__device__ __forceinline__ void cluster_sync_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
 // Arrive on an mbarrier given by its shared::cluster address (may be the peer's).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
@@ -316,6 +337,18 @@ __device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster, uint3
   asm volatile(
       "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
       ::"r"(dst_cluster), "r"(src), "r"(bytes), "r"(bar_cluster)
+      : "memory");
+}
+
+// 16-byte store into another CTA's shared memory (a shared::cluster address)
+// whose bytes complete on an mbarrier of that CTA (complete_tx), like a bulk
+// copy's: the receiver's wait on the barrier makes the data visible to it.
+__device__ __forceinline__ void st_async_cluster_v4(uint32_t cluster_addr, uint32_t a, uint32_t b,
+                                                    uint32_t c, uint32_t d, uint32_t bar_cluster) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::
+          "r"(cluster_addr),
+      "r"(a), "r"(b), "r"(c), "r"(d), "r"(bar_cluster)
       : "memory");
 }
 

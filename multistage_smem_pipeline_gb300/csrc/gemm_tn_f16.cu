@@ -199,7 +199,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   // narrowest multiple of 64 (each CTA keeps half the columns, whole 32-column
   // chunks) whose tiles fit the co-resident pairs; the ring must also hold the
   // exchange once the MMAs are done.  Chosen by itself for single-CTA plans of
-  // one wave with 512 <= K <= 1024 (measured: 1024^3).
+  // one wave with 256 <= K <= 1024 (measured: 1024^3 and 256^3).
   const int64_t tiles_1 = ((M + kBM - 1) / kBM) * ((N + bn - 1) / bn);  // the unsplit plan's
   int split_bn = 0, split_katoms = 0, split_stages = 0;
   uint32_t split_stage_bytes = 0;
@@ -242,7 +242,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   const bool split_k =
       split_bn && (o.split_k == 2 ||
                    (o.split_k == 0 && o.path == GEMM_PATH_AUTO && path == GEMM_PATH_SQUARE &&
-                    o.b_resident == 0 && M > kBM && K >= 512 && K <= 1024 && tiles_1 <= sms));
+                    o.b_resident == 0 && M > kBM && K >= 256 && K <= 1024 && tiles_1 <= sms));
   if (split_k) {
     bn = split_bn;
     path = GEMM_PATH_SQUARE;

@@ -177,6 +177,13 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
     tc_fence_after_sync();
     tmem_base = *tmem_slot;
   }
+  // The producer's L2 policies are made before the wait: they touch no
+  // memory, and the first loads need not wait for them.
+  uint64_t pol_a = 0, pol_b = 0;
+  if (warp == 0 && lane == 0) {
+    pol_b = l2_policy_evict_first();
+    pol_a = l2_policy_evict_last();
+  }
   // Set-up done without touching global memory; from here on the previous
   // kernel's results must be complete and visible.
   grid_dependency_wait();
@@ -184,8 +191,6 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const uint64_t pol_b = l2_policy_evict_first();
-      const uint64_t pol_a = l2_policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0;

@@ -120,13 +120,16 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
   cluster_sync();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  uint64_t pol_a = 0, pol_b = 0;  // the producer's L2 policies (no memory access)
+  if (warp == 0 && lane == 0) {
+    pol_a = l2_policy_evict_last();
+    pol_b = l2_policy_evict_first();
+  }
   grid_dependency_wait();  // first global-memory access follows
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer (both CTAs)
     if (lane == 0) {
-      const uint64_t pol_a = l2_policy_evict_last();
-      const uint64_t pol_b = l2_policy_evict_first();
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0;

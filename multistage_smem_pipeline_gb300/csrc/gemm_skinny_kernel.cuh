@@ -129,14 +129,17 @@ __global__ void __launch_bounds__(kSkinnyThreads, 1)
     tc_fence_after_sync();
     tmem_base = *tmem_slot;
   }
+  uint64_t pol_a = 0, pol_b = 0;  // the producer's L2 policies (no memory access)
+  if (warp == 0 && lane == 0) {
+    pol_b = l2_policy_evict_first();
+    pol_a = l2_policy_evict_last();
+  }
   grid_dependency_wait();  // first global-memory access follows
 
   const int k0 = first_k_block(t, p);
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const uint64_t pol_b = l2_policy_evict_first();
-      const uint64_t pol_a = l2_policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0;

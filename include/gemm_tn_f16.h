@@ -144,6 +144,16 @@ typedef struct {
                           an N x K B, an fp32 accumulator and aligned D rows;
                           results differ from the unsplit sum only in fp32
                           rounding (bit-exact where the partial sums are). */
+  int multicast;       /* split-K only: 0 = choose, 1 = never, 2 = always (else
+                          GEMM_ERR_INVALID_VALUE).  The cluster then also holds
+                          the next n-tile and/or m-tile (4 or 8 CTAs); the CTAs of
+                          one k-half that share an A or B block each load half of
+                          it for both by TMA multicast, so each SM fetches half the
+                          operand bytes it receives.  Chosen by itself with
+                          partners along both n and m (8 CTAs) when every cluster
+                          fits on the GPU at once; asked for, a 4-CTA cluster is
+                          taken when 8 do not fit.  Results are bit-identical to
+                          the pair form.  Not combined with `check`. */
 } gemm_options_t;
 
 /* gemm_tn_f16 with an explicit configuration (sweeps, tests).  Same
@@ -245,6 +255,8 @@ typedef struct {
                           output tiles; the grid is sized by units) */
   int small_m;         /* 1: the small-M kernel (one tile per CTA) */
   int split_k;         /* 1: k split over a CTA pair (ctas = 2 x tiles) */
+  int cluster;         /* CTAs per thread-block cluster: 1, 2 (pairs, split K), or 4
+                          or 8 (split K with multicast operands) */
 } gemm_config_t;
 int gemm_query_config(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt,
                       gemm_config_t* out);

@@ -38,14 +38,15 @@ class GemmOptions(ctypes.Structure):
                 ("timeout_ns", ctypes.c_uint64), ("inject", ctypes.c_int), ("katoms", ctypes.c_int),
                 ("epi_warps", ctypes.c_int), ("b_layout", ctypes.c_int), ("acc_f16", ctypes.c_int),
                 ("b_resident", ctypes.c_int), ("pdl", ctypes.c_int), ("wide", ctypes.c_int),
-                ("small_m", ctypes.c_int), ("check", ctypes.c_int), ("split_k", ctypes.c_int)]
+                ("small_m", ctypes.c_int), ("check", ctypes.c_int), ("split_k", ctypes.c_int),
+                ("multicast", ctypes.c_int)]
 
 
 class GemmConfig(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in ("path", "bm", "bn", "bk", "kstage", "ctas", "group_m",
                                             "tiles", "smem_bytes", "tmem_cols", "katoms",
                                             "epi_warps", "b_resident", "pdl", "wide",
-                                            "small_m", "split_k")]
+                                            "small_m", "split_k", "cluster")]
 
 
 class GemmError(RuntimeError):
@@ -109,11 +110,11 @@ def _stream_handle(stream) -> int:
 
 def _options(path=0, bn=0, kstage=0, max_ctas=0, group_m=0, timeout_ns=0, inject=0,
              katoms=0, epi_warps=0, b_layout=0, acc_f16=0, b_resident=0,
-             pdl=0, wide=0, small_m=0, check=0, split_k=0) -> GemmOptions:
+             pdl=0, wide=0, small_m=0, check=0, split_k=0, multicast=0) -> GemmOptions:
     return GemmOptions(int(path), int(bn), int(kstage), int(max_ctas), int(group_m),
                        int(timeout_ns), int(inject), int(katoms), int(epi_warps), int(b_layout),
                        int(acc_f16), int(b_resident), int(pdl), int(wide), int(small_m),
-                       int(check), int(split_k))
+                       int(check), int(split_k), int(multicast))
 
 
 def _check_operands(a: torch.Tensor, b: torch.Tensor, out):
@@ -150,8 +151,8 @@ def gemm_tn_f16(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = Non
 def gemm_tn_f16_ex(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = None, stream=None,
                    **opts) -> torch.Tensor:
     """gemm_tn_f16 with explicit options: path, bn, kstage, max_ctas, group_m, timeout_ns,
-    inject, katoms, epi_warps, acc_f16, b_resident, pdl, wide, small_m, check, split_k (the
-    fields of gemm_options_t)."""
+    inject, katoms, epi_warps, acc_f16, b_resident, pdl, wide, small_m, check, split_k,
+    multicast (the fields of gemm_options_t)."""
     M, N, K, out = _check_operands(a, b, out)
     o = _options(**opts)
     with torch.cuda.device(a.device):

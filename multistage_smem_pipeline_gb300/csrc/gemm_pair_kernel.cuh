@@ -247,6 +247,16 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
       }
       umma_commit_pair_mc(drain_bar, 0x1);
       wait_timed(drain_bar, 0, p.timeout_ns);
+      // Every epilogue warp of both CTAs has released its last accumulator
+      // (the two waits a next unit would make): their remote arrivals on this
+      // CTA's barriers have all landed before the pair's final barrier.
+      for (int j = 0; j < 2; ++j) {
+        wait_timed(tempty_bar(acc), acc_phase ^ 1u, p.timeout_ns);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
     }
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
@@ -392,7 +402,9 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
 
   __syncwarp();
   tc_fence_before_sync();
-  cluster_sync();  // no remote arrive or multicast commit targets a CTA that has left
+  // No remote arrive or commit still targets either CTA (the MMA thread has
+  // seen the last ones land), so the arrive need not wait for the D stores.
+  cluster_sync_relaxed();
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc_pair(tmem_base, p.tmem_cols);

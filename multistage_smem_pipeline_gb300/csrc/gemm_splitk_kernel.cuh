@@ -86,7 +86,16 @@ __device__ __forceinline__ uint32_t splitk_chunk_offset(int c, int q) {
 }
 
 // kCheck: the pipeline invariant check (as in gemm_tn_f16_persistent).
-template <bool kCheck = false>
+// kMcN, kMcM: 2 to put the next n-tile (m-tile) in the same cluster.  The CTAs
+// of one k-half whose tiles share a block of A (same m-block) then each load
+// half of its rows for both by TMA multicast, and likewise for B: each SM
+// fetches half the bytes it receives.  Every CTA's ring slot is then written
+// by its multicast partners too, so a slot is free only when every CTA that
+// writes into it has consumed it: each MMA commit arrives on the empty
+// barrier of the CTA itself and of its partners, and each empty barrier
+// counts one arrival per CTA.  The host passes the grid of cluster tiles
+// (kMcM x kMcN tiles each) in num_m_blocks and num_n_blocks.
+template <bool kCheck = false, int kMcN = 1, int kMcM = 1>
 __global__ void __launch_bounds__(kSplitThreads, 1)
     gemm_tn_f16_splitk(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB,
@@ -100,14 +109,28 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  static_assert((kMcN == 1 || kMcN == 2) && (kMcM == 1 || kMcM == 2), "1 or 2 tiles per dimension");
+  constexpr int kClusterCtas = 2 * kMcN * kMcM;
+  constexpr bool kMc = kClusterCtas > 2;
   const uint32_t rank = cluster_ctarank();
-  const uint32_t peer = rank ^ 1u;
+  const uint32_t kr = rank & 1u;                           // this CTA's k-half
+  const uint32_t peer = rank ^ 1u;                         // the other k-half of this tile
+  const uint32_t a_mate = rank ^ 2u;                       // kMcN: same m-block, next n-block
+  const uint32_t b_mate = rank ^ (kMcN == 2 ? 4u : 2u);    // kMcM: same n-block, next m-block
+  const int jn = kMcN == 2 ? static_cast<int>((rank >> 1) & 1u) : 0;
+  const int jm = kMcM == 2 ? static_cast<int>((rank >> (kMcN == 2 ? 2 : 1)) & 1u) : 0;
+  const uint16_t a_mask = static_cast<uint16_t>((1u << rank) | (1u << a_mate));
+  const uint16_t b_mask = static_cast<uint16_t>((1u << rank) | (1u << b_mate));
+  const uint16_t commit_mask = static_cast<uint16_t>(
+      (1u << rank) | (kMcN == 2 ? 1u << a_mate : 0u) | (kMcM == 2 ? 1u << b_mate : 0u));
   int mb, nb;
-  tile_coords(static_cast<int>(blockIdx.x >> 1), p, mb, nb);
-  // this CTA's k-blocks: the first ceil(nk/2) for rank 0, the rest for rank 1
+  tile_coords(static_cast<int>(blockIdx.x / kClusterCtas), p, mb, nb);
+  mb = mb * kMcM + jm;
+  nb = nb * kMcN + jn;
+  // this CTA's k-blocks: the first ceil(nk/2) for k-half 0, the rest for k-half 1
   const int h0 = (p.num_k_blocks + 1) / 2;
-  const int kb_lo = rank ? h0 : 0;
-  const int nkb = rank ? p.num_k_blocks - h0 : h0;
+  const int kb_lo = kr ? h0 : 0;
+  const int nkb = kr ? p.num_k_blocks - h0 : h0;
   const uint32_t bars = base + L.bars;
   auto full_bar = [&](int s) { return bars + 8u * s; };
   auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
@@ -122,12 +145,12 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     grid_launch_dependents();  // see gemm_tn_f16_persistent
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(empty_bar(s), 1 + (kMcN == 2) + (kMcM == 2));  // one commit per writing CTA
     }
     mbar_init(tfull_bar, 1);
     mbar_init(drain_bar, 1);
     mbar_init(rx_full_bar, 1);
-    // the peer's bulk copies of this CTA's half complete these bytes
+    // the peer's remote stores of this CTA's half complete these bytes
     mbar_arrive_expect_tx(rx_full_bar, static_cast<uint32_t>(p.bn) * 256u);
     init_abort_state(abort_flag, p);
     fence_barrier_init();
@@ -138,7 +161,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     tma_prefetch_desc(&tmD);
   }
   __syncwarp();
-  cluster_sync();  // both CTAs' barriers exist before any remote arrive
+  cluster_sync();  // every CTA's barriers exist before any remote arrive or multicast
   uint32_t tmem_base = 0;
   if (warp != 0) {
     if (warp == 1) {
@@ -168,9 +191,18 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
         mbar_arrive_expect_tx(full_bar(stage), p.stage_bytes);
         if (!(p.inject == 1 && issued == 0)) {
           for (int at = 0; at < p.katoms; ++at) {
-            const int x = (kb * p.katoms + at) * kBK;  // past K: the box reads zeros
-            tma_load_2d(a_dst + at * kABytes, &tmA, full_bar(stage), x, mb * kBM);
-            tma_load_2d(b_dst + at * p.b_atom_bytes, &tmB, full_bar(stage), x, nb * p.bn);
+            const int x = (kb * p.katoms + at) * kBK;  // past K (or M, N): the box reads zeros
+            const uint32_t ad = a_dst + at * kABytes, bd = b_dst + at * p.b_atom_bytes;
+            if (kMcN == 2)  // rows jn * 64 .. +64 of the A block, for this CTA and its a-mate
+              tma_load_2d_mc(ad + jn * (kABytes / 2), &tmA, full_bar(stage), x,
+                             mb * kBM + jn * (kBM / 2), a_mask);
+            else
+              tma_load_2d(ad, &tmA, full_bar(stage), x, mb * kBM);
+            if (kMcM == 2)  // rows jm * BN/2 .. of the B block, for this CTA and its b-mate
+              tma_load_2d_mc(bd + jm * (p.b_atom_bytes / 2), &tmB, full_bar(stage), x,
+                             nb * p.bn + jm * (p.bn / 2), b_mask);
+            else
+              tma_load_2d(bd, &tmB, full_bar(stage), x, nb * p.bn);
           }
         }
         ++issued;
@@ -182,6 +214,11 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
       const uint32_t first = issued > static_cast<uint32_t>(S) ? issued - S : 0u;
       for (uint32_t i = first; i < issued; ++i)
         wait_timed(full_bar(i % S), (i / S) & 1u, p.timeout_ns);
+      // The partners' commits on this CTA's empty barriers have landed before
+      // the cluster's final barrier (their last phases complete).
+      if (kMc)
+        for (uint32_t i = first; i < issued; ++i)
+          wait_timed(empty_bar(i % S), (i / S) & 1u, p.timeout_ns);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -205,7 +242,10 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
           for (int k = 0; k < kBK / kUmmaK; ++k)
             umma_f16(tmem_base, a_desc + 2u * k, b_desc + 2u * k, p.idesc, (i | at | k) != 0);
         }
-        umma_commit(empty_bar(stage));
+        if (kMc)
+          umma_commit_mc(empty_bar(stage), commit_mask);
+        else
+          umma_commit(empty_bar(stage));
         if (++stage == S) {
           stage = 0;
           phase ^= 1u;
@@ -240,7 +280,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
         const uint32_t off = splitk_chunk_offset(c, q);
         uint32_t r[32];
         if (rows_live) {
-          tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(peer * half + c * kEpiCols), r);
+          tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>((kr ^ 1u) * half + c * kEpiCols), r);
           tmem_ld_wait();
         } else {  // rows past M: the peer stores nothing there, but the bytes are counted
 #pragma unroll
@@ -257,12 +297,12 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
       if (__all_sync(0xffffffffu, wait_cluster_or_abort(rx_full_bar, 0, p.timeout_ns, abort_flag,
                                                         kSiteTmemFull)) &&
           rows_live) {
-        const int n0 = nb * p.bn + static_cast<int>(rank) * half;
+        const int n0 = nb * p.bn + static_cast<int>(kr) * half;
         const int nchunks = (min(half, p.N - n0) + kEpiCols - 1) / kEpiCols;
         int seq = 0;
         for (int c = sel; c < nchunks; c += 2, ++seq) {
           uint32_t r[32];
-          tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(rank * half + c * kEpiCols), r);
+          tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(kr * half + c * kEpiCols), r);
           tmem_ld_wait();
 #pragma unroll
           for (int g = 0; g < 8; ++g) {
@@ -309,8 +349,9 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
 
   __syncwarp();
   tc_fence_before_sync();
-  // Each CTA has seen the peer's copy land (rx-full) before it gets here, so
-  // no copy targets a CTA that has left; the arrive need not wait for the D
+  // Each CTA has seen the peer's partial land (rx-full), and with multicast
+  // its partners' bytes (full) and commits (empty), before it gets here, so
+  // nothing targets a CTA that has left; the arrive need not wait for the D
   // stores.
   cluster_sync_relaxed();
   if (warp == 1) {

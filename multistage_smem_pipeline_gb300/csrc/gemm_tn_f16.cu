@@ -26,6 +26,8 @@ struct DeviceState {
   int smem_attr = 0;       // dynamic smem granted to the single-CTA kernel
   int pair_smem_attr = 0;  // ... and to the pair kernel
   int max_pairs = 0;       // co-resident 2-CTA clusters at full shared memory
+  int max_quads = 0;       // ... 4-CTA clusters (split K with multicast)
+  int max_octs = 0;        // ... 8-CTA clusters
 };
 
 namespace {
@@ -114,10 +116,11 @@ uint32_t stage_bytes_for(int path, int bn, int katoms = 1, int nt = 1) {
 struct Plan {
   gemm_config_t cfg;
   GemmParams p;
+  int mc_n, mc_m;  // split K: tiles per cluster along n and m (multicast operands)
 };
 
 int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sms, int max_pairs,
-              Plan* out, int b_kn = 0, bool direct_d = false) {
+              int max_quads, int max_octs, Plan* out, int b_kn = 0, bool direct_d = false) {
   gemm_options_t o;
   std::memset(&o, 0, sizeof(o));
   if (opt) o = *opt;
@@ -126,11 +129,13 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
       o.inject > 2 || o.katoms < 0 || o.katoms > 2 || o.acc_f16 < 0 || o.acc_f16 > 1 ||
       o.b_resident < 0 || o.b_resident > 2 || o.pdl < 0 || o.pdl > 1 || o.wide < 0 ||
       o.wide > 2 || o.small_m < 0 || o.small_m > 2 || o.split_k < 0 || o.split_k > 2 ||
-      o.check < 0 || o.check > 1 ||
+      o.check < 0 || o.check > 1 || o.multicast < 0 || o.multicast > 2 ||
       (o.epi_warps != 0 && o.epi_warps != 4 && o.epi_warps != 8))
     return GEMM_ERR_INVALID_VALUE;
   if (o.path == GEMM_PATH_SKINNY && M > kBM) return GEMM_ERR_INVALID_VALUE;
   if (max_pairs < 1) max_pairs = std::max(1, sms / 2);
+  if (max_quads < 1) max_quads = std::max(1, sms / 4);
+  if (max_octs < 1) max_octs = std::max(1, sms / 8);
 
   // Candidates: (path, bn, tiles per unit).  Cost = waves of units x
   // k-blocks x per-k-block cost; ties go to the pair path, then to wide
@@ -260,6 +265,34 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   const int64_t num_n = (N + bn - 1) / bn;
   const int64_t tiles = num_m * num_n;
   if (tiles > INT_MAX) return GEMM_ERR_INVALID_VALUE;
+  // Split K with multicast operands: the cluster also holds the next n-tile
+  // and/or m-tile, and the CTAs of a k-half that share a block of A (B) each
+  // fetch half of it for both.  Every cluster must be resident at once (one
+  // wave).  Chosen by itself only with partners on both sides (8 CTAs, A and
+  // B both halved): 256^3 3.99 -> 3.85 us, 512^3 even; 1024^3 on 4-CTA
+  // clusters (all that fit at once there) was 6.77 -> 6.85 us, same box.
+  // With multicast = 2 a 4-CTA cluster is taken when 8 do not fit.
+  int mc_n = 1, mc_m = 1;
+  if (o.multicast == 2 && (!split_k || o.check)) return GEMM_ERR_INVALID_VALUE;
+  if (split_k && o.multicast != 1 && !o.check) {
+    const auto fits = [&](int cn, int cm) {
+      const int size = 2 * cn * cm;
+      int64_t cap = size == 8 ? max_octs : size == 4 ? max_quads : max_pairs;
+      if (o.max_ctas) cap = std::min<int64_t>(cap, o.max_ctas / size);
+      return ((num_m + cm - 1) / cm) * ((num_n + cn - 1) / cn) <= cap;
+    };
+    const int cn = num_n >= 2 ? 2 : 1, cm = num_m >= 2 ? 2 : 1;
+    if (fits(cn, cm) && (o.multicast == 2 || cn * cm == 4)) {
+      mc_n = cn;
+      mc_m = cm;
+    } else if (o.multicast == 2 && cn == 2 && fits(2, 1)) {
+      mc_n = 2;
+    } else if (o.multicast == 2 && cm == 2 && fits(1, 2)) {
+      mc_m = 2;
+    }
+    if (o.multicast == 2 && mc_n * mc_m == 1) return GEMM_ERR_INVALID_VALUE;
+  }
+  const int64_t packed_m = (num_m + mc_m - 1) / mc_m, packed_n = (num_n + mc_n - 1) / mc_n;
   // Wide pair units: two adjacent n-tiles per unit share each A slice, so a
   // one-slice stage feeds twice the MMA work and the ring gets deeper (more
   // lookahead against DRAM latency) in the same shared memory.
@@ -372,7 +405,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   };
   int ctas;
   if (split_k) {
-    ctas = static_cast<int>(2 * tiles);  // a CTA pair for each tile
+    ctas = static_cast<int>(2 * mc_n * mc_m * packed_m * packed_n);  // a CTA pair for each tile
   } else if (small_m) {
     ctas = static_cast<int>(tiles);  // one tile each
   } else if (path == GEMM_PATH_PAIR) {
@@ -408,6 +441,9 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   pl.cfg.wide = wide ? 1 : 0;
   pl.cfg.small_m = small_m ? 1 : 0;
   pl.cfg.split_k = split_k ? 1 : 0;
+  pl.cfg.cluster = split_k ? 2 * mc_n * mc_m : (path == GEMM_PATH_PAIR ? 2 : 1);
+  pl.mc_n = mc_n;
+  pl.mc_m = mc_m;
 
   GemmParams& p = pl.p;
   p.M = static_cast<int32_t>(M);
@@ -415,11 +451,12 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   p.K = static_cast<int32_t>(K);
   p.bn = bn;
   p.stages = stages;
-  p.num_m_blocks = static_cast<int32_t>(num_m);
-  // the kernel schedules units: with wide units, pairs of adjacent n-tiles
-  p.num_n_blocks = static_cast<int32_t>(units_n);
+  // the kernel schedules units: with wide units, pairs of adjacent n-tiles;
+  // with split K, clusters of mc_m x mc_n tiles
+  p.num_m_blocks = static_cast<int32_t>(split_k ? packed_m : num_m);
+  p.num_n_blocks = static_cast<int32_t>(split_k ? packed_n : units_n);
   p.num_k_blocks = static_cast<int32_t>(num_k);
-  p.num_tiles = static_cast<int32_t>(units);
+  p.num_tiles = static_cast<int32_t>(split_k ? packed_m * packed_n : units);
   p.group_m = group_m;
   p.idesc = make_idesc(bm, bn) | (b_kn ? (1u << 16) : 0u);  // bit 16: B is MN-major
   if (o.acc_f16) p.idesc &= ~(3u << 4);                      // bits 4-5: D format F16
@@ -468,6 +505,8 @@ bool grant_smem(Kernel k) {
 template <bool kDirectD>
 bool grant_all(bool ok) {
   return ok && grant_smem(gemm_tn_f16_skinny<kDirectD>) && grant_smem(gemm_tn_f16_splitk<>) &&
+         grant_smem(gemm_tn_f16_splitk<false, 2, 1>) && grant_smem(gemm_tn_f16_splitk<false, 1, 2>) &&
+         grant_smem(gemm_tn_f16_splitk<false, 2, 2>) &&
          grant_smem(gemm_tn_f16_persistent<4, false, kDirectD>) &&
          grant_smem(gemm_tn_f16_persistent<8, false, kDirectD>) &&
          grant_smem(gemm_tn_f16_persistent<4, true, kDirectD>) &&
@@ -517,6 +556,15 @@ cudaError_t launch_checked(const cudaLaunchConfig_t& cfg, bool pair, bool wide, 
   return epi_warps == 8
              ? cudaLaunchKernelEx(&cfg, gemm_tn_f16_persistent<8, false, false, true>, a, b, d, p)
              : cudaLaunchKernelEx(&cfg, gemm_tn_f16_persistent<4, false, false, true>, a, b, d, p);
+}
+
+cudaError_t launch_splitk(const cudaLaunchConfig_t& cfg, int mc_n, int mc_m, const CUtensorMap& a,
+                          const CUtensorMap& b, const CUtensorMap& d, const GemmParams& p) {
+  if (mc_n == 2 && mc_m == 2)
+    return cudaLaunchKernelEx(&cfg, gemm_tn_f16_splitk<false, 2, 2>, a, b, d, p);
+  if (mc_n == 2) return cudaLaunchKernelEx(&cfg, gemm_tn_f16_splitk<false, 2, 1>, a, b, d, p);
+  if (mc_m == 2) return cudaLaunchKernelEx(&cfg, gemm_tn_f16_splitk<false, 1, 2>, a, b, d, p);
+  return cudaLaunchKernelEx(&cfg, gemm_tn_f16_splitk<>, a, b, d, p);
 }
 
 template <bool kDirectD, int kNT, bool kScaled>
@@ -583,6 +631,26 @@ int prepare_device(DeviceState* st) {
     clusters = st->sm_count / 2;
   }
   st->max_pairs = std::min(clusters, st->sm_count / 2);
+  // co-resident 4- and 8-CTA clusters of the split-K kernel
+  cfg.blockDim = dim3(kSplitThreads, 1, 1);
+  attr[0].val.clusterDim.x = 4;
+  cfg.gridDim = dim3(4 * (st->sm_count / 4), 1, 1);
+  if (cudaOccupancyMaxActiveClusters(&clusters, gemm_tn_f16_splitk<false, 2, 1>, &cfg) !=
+          cudaSuccess ||
+      clusters < 0) {
+    cudaGetLastError();
+    clusters = 0;  // multicast split K then uses 2-CTA clusters only
+  }
+  st->max_quads = std::min(clusters, st->sm_count / 4);
+  attr[0].val.clusterDim.x = 8;
+  cfg.gridDim = dim3(8 * (st->sm_count / 8), 1, 1);
+  if (cudaOccupancyMaxActiveClusters(&clusters, gemm_tn_f16_splitk<false, 2, 2>, &cfg) !=
+          cudaSuccess ||
+      clusters < 0) {
+    cudaGetLastError();
+    clusters = 0;
+  }
+  st->max_octs = std::min(clusters, st->sm_count / 8);
   return GEMM_OK;
 }
 
@@ -699,7 +767,8 @@ int launch_gemm(int64_t M, int64_t N, int64_t K, const View& a, const View& b, c
   int rc;
   if ((rc = prepare_device(st)) != GEMM_OK) return rc;
   Plan pl;
-  rc = make_plan(M, N, K, opt, st->sm_count, st->max_pairs, &pl, b_kn, d_direct != nullptr);
+  rc = make_plan(M, N, K, opt, st->sm_count, st->max_pairs, st->max_quads, st->max_octs, &pl, b_kn,
+                 d_direct != nullptr);
   if (rc != GEMM_OK) return rc;
   if ((rc = get_encoder()) != GEMM_OK) return rc;
   pl.p.ldc = ldc;
@@ -712,11 +781,14 @@ int launch_gemm(int64_t M, int64_t N, int64_t K, const View& a, const View& b, c
   }
 
   const bool pair = pl.cfg.path == GEMM_PATH_PAIR;
-  const uint32_t b_box_rows = pair ? pl.cfg.bn / 2 : pl.cfg.bn;
+  // a pair CTA loads half of B; a multicast split-K CTA half of the block it shares
+  const uint32_t b_box_rows = (pair || pl.mc_m == 2) ? pl.cfg.bn / 2 : pl.cfg.bn;
+  const uint32_t a_box_rows = pl.mc_n == 2 ? kBM / 2 : kBM;
   CUtensorMap tmA, tmB, tmD;
   const int b_rc = b_kn ? encode_2d(&tmB, b, 64, kBK, CU_TENSOR_MAP_SWIZZLE_128B)
                         : encode_2d(&tmB, b, kBK, b_box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
-  if (encode_2d(&tmA, a, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B) != GEMM_OK || b_rc != GEMM_OK)
+  if (encode_2d(&tmA, a, kBK, a_box_rows, CU_TENSOR_MAP_SWIZZLE_128B) != GEMM_OK ||
+      b_rc != GEMM_OK)
     return GEMM_ERR_INVALID_VALUE;
   if (d_direct) {  // plain stores to D; the kernel never reads tmD
     pl.p.D = d_direct;
@@ -738,9 +810,9 @@ int launch_gemm(int64_t M, int64_t N, int64_t K, const View& a, const View& b, c
     attr[nattr].val.programmaticStreamSerializationAllowed = 1;
     ++nattr;
   }
-  if (pair || pl.cfg.split_k) {
+  if (pl.cfg.cluster > 1) {
     attr[nattr].id = cudaLaunchAttributeClusterDimension;
-    attr[nattr].val.clusterDim.x = 2;
+    attr[nattr].val.clusterDim.x = static_cast<unsigned>(pl.cfg.cluster);
     attr[nattr].val.clusterDim.y = 1;
     attr[nattr].val.clusterDim.z = 1;
     ++nattr;
@@ -757,7 +829,7 @@ int launch_gemm(int64_t M, int64_t N, int64_t K, const View& a, const View& b, c
   const cudaError_t e =
       pl.p.check ? launch_checked(cfg, pair, wide, res, small, pl.cfg.split_k != 0,
                                   pl.cfg.epi_warps, tmA, tmB, tmD, pl.p) :
-      pl.cfg.split_k ? cudaLaunchKernelEx(&cfg, gemm_tn_f16_splitk<>, tmA, tmB, tmD, pl.p) :
+      pl.cfg.split_k ? launch_splitk(cfg, pl.mc_n, pl.mc_m, tmA, tmB, tmD, pl.p) :
       d_direct ? launch_kernel<true>(cfg, pair, wide, res, small, pl.cfg.epi_warps, tmA, tmB, tmD,
                                      pl.p)
                : launch_kernel<false>(cfg, pair, wide, res, small, pl.cfg.epi_warps, tmA, tmB,
@@ -774,7 +846,7 @@ int check_options(const gemm_options_t* opt, int b_kn, int64_t M, int64_t N, int
   if (!opt) return GEMM_OK;
   Plan tmp;
   return make_plan(std::max<int64_t>(M, 1), std::max<int64_t>(N, 8), std::max<int64_t>(K, 8), opt,
-                   148, 74, &tmp, b_kn);
+                   148, 74, 37, 18, &tmp, b_kn);
 }
 
 namespace {
@@ -827,18 +899,20 @@ extern "C" int gemm_query_config(int64_t M, int64_t N, int64_t K, const gemm_opt
                                  gemm_config_t* out) {
   if (!out || M <= 0 || N <= 0 || K <= 0 || M > INT_MAX || N > INT_MAX || K > INT_MAX)
     return GEMM_ERR_INVALID_VALUE;
-  int sms = 148, pairs = 74, dev = 0;
+  int sms = 148, pairs = 74, quads = 37, octs = 18, dev = 0;
   DeviceState* st = nullptr;
   if (current_device(&dev, &st) == GEMM_OK && prepare_device(st) == GEMM_OK) {
     sms = st->sm_count;
     pairs = st->max_pairs;
+    quads = st->max_quads;
+    octs = st->max_octs;
   } else {
     cudaGetLastError();
   }
   const int b_kn = opt ? opt->b_layout : 0;
   if (b_kn != 0 && b_kn != 1) return GEMM_ERR_INVALID_VALUE;
   Plan pl;
-  const int rc = make_plan(M, N, K, opt, sms, pairs, &pl, b_kn);
+  const int rc = make_plan(M, N, K, opt, sms, pairs, quads, octs, &pl, b_kn);
   if (rc == GEMM_OK) *out = pl.cfg;
   return rc;
 }

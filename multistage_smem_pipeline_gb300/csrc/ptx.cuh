@@ -411,6 +411,28 @@ __device__ __forceinline__ void umma_f16_pair(uint32_t d_tmem, uint64_t a_desc, 
 
 // Arrive once, when the pair's MMAs issued so far complete, on the mbarrier at
 // offset `bar` in every CTA of `cta_mask`.
+// TMA load of one box into the shared memory of every CTA of the cluster in
+// `cta_mask` (at the same offset), each CTA's barrier at `bar`'s offset
+// counting the bytes it receives.  Only for tensors in this GPU's memory.
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void* tmap, uint32_t bar,
+                                               int32_t x, int32_t y, uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "h"(cta_mask)
+      : "memory");
+}
+
+// tcgen05.commit of this CTA's MMAs arriving on the barrier at `bar`'s offset
+// in every CTA of the cluster in `cta_mask`.
+__device__ __forceinline__ void umma_commit_mc(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
+}
+
 __device__ __forceinline__ void umma_commit_pair_mc(uint32_t bar, uint16_t cta_mask) {
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"

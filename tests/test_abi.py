@@ -105,7 +105,8 @@ def test_rejects_bad_options(binding):
                dict(b_resident=2, path=binding.PATH_PAIR),
                dict(b_resident=2, bn=32, group_m=4), dict(wide=3), dict(wide=-1),
                dict(wide=2, path=binding.PATH_SQUARE), dict(check=2), dict(check=-1),
-               dict(split_k=3), dict(small_m=3)]:
+               dict(split_k=3), dict(small_m=3), dict(multicast=3), dict(multicast=-1),
+               dict(multicast=2, split_k=1)]:
         o = binding._options(**kw)
         M = 256 if kw.get("path") == binding.PATH_SKINNY else 64
         assert _call(binding, P0, P1, P2, M, 64, 64, o) == binding.GEMM_ERR_INVALID_VALUE, kw

@@ -39,14 +39,23 @@ def _check(cfg, M, N, K):
     bm = 256 if cfg["path"] == 3 else 128
     assert cfg["bm"] == bm
     assert cfg["tiles"] == -(-M // bm) * -(-N // cfg["bn"])
-    assert 1 <= cfg["ctas"] <= cfg["tiles"] * (2 if (cfg["path"] == 3 or cfg["split_k"]) else 1)
     if cfg["split_k"]:
-        assert cfg["ctas"] == 2 * cfg["tiles"] and cfg["bn"] % 64 == 0 and cfg["path"] == 1
+        # clusters of 2 (one tile), 4 or 8 (1 x 2, 2 x 1 or 2 x 2 tiles, operands multicast);
+        # a ragged edge still gets whole clusters
+        nm, nn = -(-M // 128), -(-N // cfg["bn"])
+        packs = {2: [(1, 1)], 4: [(2, 1), (1, 2)], 8: [(2, 2)]}[cfg["cluster"]]
+        assert cfg["ctas"] in [cfg["cluster"] * -(-nm // cm) * -(-nn // cn) for cm, cn in packs]
+        assert cfg["cluster"] != 8 or (nm >= 2 and nn >= 2)     # a partner on both sides
+        assert cfg["cluster"] != 4 or nm >= 2 or nn >= 2
+        assert cfg["bn"] % 64 == 0 and cfg["path"] == 1
         assert cfg["epi_warps"] == 8 and not cfg["b_resident"] and not cfg["small_m"]
         # the ring holds the eight warps' staging buffers once the MMAs are done, and the
         # peer's 128 x bn/2 fp32 partial has a region of its own
         ring = cfg["kstage"] * cfg["katoms"] * (128 + cfg["bn"]) * 128
-        assert ring >= 32768 + 256 * cfg["bn"] and cfg["smem_bytes"] >= ring + 256 * cfg["bn"]
+        assert ring >= 32768 and cfg["smem_bytes"] >= ring + 256 * cfg["bn"]
+    else:
+        assert 1 <= cfg["ctas"] <= cfg["tiles"] * (2 if cfg["path"] == 3 else 1)
+        assert cfg["cluster"] == (2 if cfg["path"] == 3 else 1)
     if cfg["path"] == 3:
         assert cfg["ctas"] % 2 == 0                                    # whole clusters of 2
     if cfg["path"] == 2:
@@ -68,7 +77,7 @@ def _check(cfg, M, N, K):
         work = -(-M // 256) * (-(-num_n // 2) if cfg["wide"] else num_n)
         slots, step = cfg["ctas"] // 2, 1
     elif cfg["split_k"]:
-        work, slots, step = cfg["tiles"], cfg["ctas"] // 2, 1
+        return  # one cluster per tile group: nothing to balance
     else:
         work, slots = cfg["tiles"], cfg["ctas"]
         step = -(-N // cfg["bn"]) if cfg["b_resident"] else 1
@@ -87,7 +96,9 @@ def test_default_plans_fit(binding):
                                   dict(wide=2), dict(wide=2, path=3, epi_warps=8),
                                   dict(wide=1), dict(small_m=1), dict(small_m=2),
                                   dict(small_m=2, katoms=1), dict(split_k=1), dict(split_k=2),
-                                  dict(split_k=2, katoms=1), dict(split_k=2, bn=256)])
+                                  dict(split_k=2, katoms=1), dict(split_k=2, bn=256),
+                                  dict(split_k=2, multicast=1), dict(split_k=2, multicast=2),
+                                  dict(split_k=2, multicast=2, max_ctas=32)])
 def test_forced_plans_fit_or_are_refused(binding, opts):
     accepted = 0
     for M, N, K in _shapes(600, 502 + len(str(opts))):
@@ -112,6 +123,8 @@ def test_forced_plans_fit_or_are_refused(binding, opts):
             assert cfg["wide"] == 0
         if "split_k" in opts:
             assert cfg["split_k"] == (1 if opts["split_k"] == 2 else 0)
+        if "multicast" in opts:
+            assert cfg["split_k"] == 1 and (cfg["cluster"] > 2) == (opts["multicast"] == 2)
         if "small_m" in opts:
             assert cfg["small_m"] == (1 if opts["small_m"] == 2 else 0)
         if opts.get("b_resident") == 1:

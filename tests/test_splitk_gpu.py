@@ -3,7 +3,10 @@ through the C-ABI.  A cluster of two CTAs computes each 128 x bn tile, each
 CTA half of the k range; the two exchange their fp32 partials through
 distributed shared memory and each rounds and stores half of the tile.  The
 sum differs from a single accumulator's only in fp32 rounding, so the usual
-bound applies, and integer-valued inputs must still match bit for bit."""
+bound applies, and integer-valued inputs must still match bit for bit.  With
+multicast operands a cluster holds two or four such tiles, and the CTAs that
+share a block of A or B each load half of it for both: the MMAs and the sums
+are the same, so the results must equal the 2-CTA form's bit for bit."""
 import numpy as np
 import pytest
 import torch
@@ -143,6 +146,64 @@ def test_stalled_stage_times_out_and_context_survives(lib, gpu):
     assert (raw >> 8) in (1, 2, 3, 4)
     for _ in range(2):
         d = lib.gemm_tn_f16_ex(a, b, split_k=2)
+        torch.cuda.synchronize()
+        _check(d.cpu().numpy().view(np.uint16), a_bits, b_bits)
+    assert lib.get_device_error()[0] == lib.GEMM_OK
+
+
+def test_multicast_cluster_shapes(lib, gpu):
+    # chosen by itself with partners along n and m (8 CTAs), when every cluster of 8 fits
+    # at once; asked for, also along n only (one m-block) or m only (one n-block): 4
+    assert lib.query_config(1024, 1024, 1024)["cluster"] in (2, 8)
+    assert lib.query_config(256, 256, 256)["cluster"] == 8
+    assert lib.query_config(100, 1024, 1024, split_k=2)["cluster"] == 2
+    assert lib.query_config(100, 1024, 1024, split_k=2, multicast=2)["cluster"] == 4
+    assert lib.query_config(1024, 64, 1024, split_k=2, multicast=2)["cluster"] == 4
+    assert lib.query_config(100, 64, 1024, split_k=2)["cluster"] == 2
+    assert lib.query_config(1024, 1024, 1024, multicast=1)["cluster"] == 2
+    assert lib.query_config(1024, 1024, 1024, check=1)["cluster"] == 2
+    with pytest.raises(lib.GemmError):
+        lib.query_config(100, 64, 1024, split_k=2, multicast=2)   # no partner to share with
+
+
+@pytest.mark.parametrize("M,N,K", [(1024, 1024, 1024), (300, 520, 1000), (129, 264, 136),
+                                   (77, 1000, 520), (640, 384, 1088), (256, 256, 256),
+                                   (1000, 120, 512), (384, 640, 320), (136, 136, 768)])
+def test_multicast_matches_the_pair_form_bit_for_bit(lib, gpu, M, N, K):
+    a = synthetic.uniform_pm1(3 * M + K, (M, K))
+    b = synthetic.uniform_pm1(3 * N + K + 1, (N, K))
+    cfg = lib.query_config(M, N, K, split_k=2, multicast=2)
+    assert cfg["cluster"] in (4, 8)
+    print(cfg["cluster"], end=" ")
+    mc = _run(lib, a, b, gpu, split_k=2, multicast=2)
+    pair = _run(lib, a, b, gpu, split_k=2, multicast=1)
+    assert np.array_equal(mc, pair)
+    _check(mc, a, b)
+
+
+@pytest.mark.parametrize("bn,katoms,kstage", [(64, 2, 2), (128, 1, 3), (192, 1, 2), (256, 1, 2)])
+def test_multicast_tile_widths_and_ring_wrap(lib, gpu, bn, katoms, kstage):
+    # halves of B of bn / 2 rows per CTA; each CTA's k-half wraps its ring
+    M, N, K = 520, 4 * bn + 40, 2 * 64 * katoms * (2 * kstage + 1)
+    a = synthetic.gaussian(bn + kstage, (M, K))
+    b = synthetic.gaussian(bn + kstage + 1, (N, K))
+    got = _run(lib, a, b, gpu, split_k=2, multicast=2, bn=bn, katoms=katoms, kstage=kstage)
+    assert np.array_equal(got, _run(lib, a, b, gpu, split_k=2, multicast=1, bn=bn, katoms=katoms,
+                                    kstage=kstage))
+    _check(got, a, b)
+
+
+def test_multicast_stalled_stage_times_out_and_context_survives(lib, gpu):
+    a_bits = synthetic.uniform_pm1(121, (512, 1024))
+    b_bits = synthetic.uniform_pm1(122, (512, 1024))
+    a, b = _dev(a_bits, gpu), _dev(b_bits, gpu)
+    assert lib.get_device_error()[0] == lib.GEMM_OK
+    lib.gemm_tn_f16_ex(a, b, inject=1, timeout_ns=50_000_000, split_k=2, multicast=2)
+    status, raw = lib.get_device_error()
+    assert status == lib.GEMM_ERR_TIMEOUT
+    assert (raw >> 8) in (1, 2, 3, 4)
+    for _ in range(2):
+        d = lib.gemm_tn_f16_ex(a, b, split_k=2, multicast=2)
         torch.cuda.synchronize()
         _check(d.cpu().numpy().view(np.uint16), a_bits, b_bits)
     assert lib.get_device_error()[0] == lib.GEMM_OK

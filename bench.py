@@ -609,7 +609,8 @@ def bench_config(tag, binding, torch, dev, stream, l2, peaks, peak_src, clocks):
              "roofline_ms": max(flops / (float(peaks["bf16_tflops"]) * 1e12),
                                 alg_bytes / (float(peaks["hbm_gbs"]) * 1e9)) * 1e3,
              "plan": {k: cfg[k] for k in ("path", "bn", "kstage", "katoms", "ctas", "epi_warps",
-                                          "b_resident", "wide", "small_m", "split_k")},
+                                          "b_resident", "wide", "small_m", "split_k",
+                                          "cluster")},
              "l2": f"{R} operand copies ({R * int(alg_bytes) >> 20} MiB > 3 x L2) cycled",
              "clocks": clk}
     entry["roofline_frac"] = entry["roofline_ms"] / ms
@@ -935,7 +936,7 @@ def run_gpu(args, tag):
                                                             2 if cfg["wide"] else 1,
                                                             flag(scaled))
                       if cfg["path"] == 3 else
-                      "gemm_tn_f16_splitk" if cfg["split_k"] else
+                      ("gemm_tn_f16_splitk (cluster of %d)" % cfg["cluster"]) if cfg["split_k"] else
                       "gemm_tn_f16_skinny<%s>" % flag(direct_d) if cfg["small_m"] else
                       "gemm_tn_f16_persistent<%d, %s, %s>" % (cfg["epi_warps"],
                                                               flag(cfg["b_resident"]),

@@ -317,7 +317,19 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
   // of the bytes per 128 x 256 tile when K = N = 256.  With a few n-blocks,
   // tiles are ordered n-fastest (group_m = 1) over a grid that is a multiple
   // of num_n, so CTA c only ever meets n-block c % num_n.  Used when each CTA
-  // has at least two tiles and the ring still gets 3 stages of A.
+  // has at least two tiles, the ring still gets 3 stages of A, and it keeps
+  // more of A in flight than the streamed plan's ring would (A streams from
+  // DRAM; B in shared memory takes room from A's ring) -- or as much, with
+  // several n-blocks (with one, streamed B is an L2 hit for every tile).
+  // Chosen by itself with the streamed plan's epilogue warps only (four
+  // warps' deeper ring did not pay: 81920x256x256 18.31 against 18.25 us with
+  // eight).  Measured, same box, resident against streamed: 81920x1024x128
+  // 32.8 / 34.3 us (128 against 64 KiB of A in flight), 65536x128x512 20.5 /
+  // 17.3 (64 against 96), 81920x512x256 27.1 / 27.4 (equal, 2 n-blocks),
+  // 81920x256x256 18.25 / 18.12 (equal, 1 n-block).
+  const uint32_t streamed_a_in_flight =
+      static_cast<uint32_t>(stages_that_fit(stage_bytes_for(path, bn, katoms, nt), epi_warps)) *
+      katoms * kABytes;
   bool b_resident = false;
   uint32_t bres_bytes = 0;
   int64_t ctas_1 = std::min<int64_t>(tiles, sms);
@@ -336,7 +348,11 @@ int make_plan(int64_t M, int64_t N, int64_t K, const gemm_options_t* opt, int sm
         const uint32_t bres = static_cast<uint32_t>(nk) * ka * b_atom_bytes_for(path, bn);
         if (bres > static_cast<uint32_t>(kMaxDynSmem)) continue;
         const int f = stages_that_fit(static_cast<uint32_t>(ka) * kABytes, ew, bres, nk);
-        if (f >= min_stages && (ka == 1 || o.katoms || f >= 3)) {
+        const uint32_t a_in_flight = static_cast<uint32_t>(f) * ka * kABytes;
+        const bool deeper = a_in_flight > streamed_a_in_flight ||
+                            (a_in_flight == streamed_a_in_flight && num_n >= 2);
+        if (f >= min_stages && (ka == 1 || o.katoms || f >= 3) &&
+            (o.b_resident == 2 || (deeper && ew == epi_warps))) {
           b_resident = true;
           bres_bytes = bres;
           epi_warps = ew;

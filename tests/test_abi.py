@@ -272,11 +272,15 @@ def test_padded_call_without_a_device_reports_cuda_error(binding):
 
 
 def test_resident_b_plans(binding):
-    # the tall shape the multistage page times: one n-block, 640 tiles, so each
-    # CTA holds all of B (256 x 256 fp16) and streams only A
-    cfg = binding.query_config(81920, 256, 256)
+    # a tall shape whose resident B leaves A's ring deeper than streaming would:
+    # each CTA holds its n-block of B and streams only A
+    cfg = binding.query_config(81920, 1024, 128)
     assert cfg["b_resident"] == 1 and cfg["path"] == binding.PATH_SQUARE
     assert cfg["smem_bytes"] <= 232448
+    # the page's 81920 x 256 x 256: the same depth of A either way, one n-block
+    # (streamed B is an L2 hit for every tile), so B streams unless asked for
+    assert binding.query_config(81920, 256, 256)["b_resident"] == 0
+    assert binding.query_config(81920, 256, 256, b_resident=2)["b_resident"] == 1
     # off on request, and never for many n-blocks, the pair path or a K x N B
     assert binding.query_config(81920, 256, 256, b_resident=1)["b_resident"] == 0
     assert binding.query_config(8192, 8192, 8192)["b_resident"] == 0

@@ -124,12 +124,17 @@ def test_resident_scaled_and_fp16_accumulator(lib, gpu):
     assert np.array_equal(res, streamed)
 
 
-def test_tall_workloads_choose_resident(lib, gpu):
-    # the shape the multistage page times (81920 x 256 x 256) and its fp16
-    # accumulator variant run with B resident when the library chooses
+def test_tall_shapes_choose_resident_where_it_keeps_more_a_in_flight(lib, gpu):
+    # resident B when it leaves A's ring deeper than streaming B would (or as deep, with
+    # several n-blocks); the page's 81920 x 256 x 256 (one n-block, the same depth either
+    # way) and its fp16-accumulator variant stream B
+    assert lib.query_config(81920, 1024, 128)["b_resident"] == 1
+    assert lib.query_config(81920, 512, 256)["b_resident"] == 1
+    assert lib.query_config(65536, 128, 512)["b_resident"] == 0
     for tag in ("c6", "c8"):
         spec = synthetic.WORKLOADS[tag]
-        assert lib.query_config(spec["M"], spec["N"], spec["K"])["b_resident"] == 1
+        assert lib.query_config(spec["M"], spec["N"], spec["K"])["b_resident"] == 0
+        assert lib.query_config(spec["M"], spec["N"], spec["K"], b_resident=2)["b_resident"] == 1
 
 
 def test_resident_stall_times_out_and_context_survives(lib, gpu):

@@ -139,8 +139,10 @@ typedef struct {
                           Split: a cluster of two CTAs computes each 128 x bn tile,
                           each CTA half of the k range; the two exchange their fp32
                           partials through distributed shared memory and each
-                          rounds and stores half of the tile.  For short k loops
-                          whose tiles fit in one wave of CTA pairs (1024^3).  Needs
+                          rounds and stores half of the tile.  Chosen by itself
+                          for 256 <= K <= 1024 when the unsplit tiles fit in one
+                          wave and the split ones in one wave of CTA pairs
+                          (1024^3, 256^3).  Needs
                           an N x K B, an fp32 accumulator and aligned D rows;
                           results differ from the unsplit sum only in fp32
                           rounding (bit-exact where the partial sums are). */

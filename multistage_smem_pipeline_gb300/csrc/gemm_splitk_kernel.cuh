@@ -79,8 +79,8 @@ __device__ __forceinline__ bool wait_cluster_or_abort(uint32_t bar, uint32_t par
 // A partial of half a tile, 128 rows x BN/2 fp32 columns, as the epilogue
 // warps hold it: chunk c (32 columns) of lane quadrant q is 4 KiB at
 // (c * 4 + q) * 4096, in which 16-byte group g (columns 4g..4g+3) of row
-// q * 32 + lane lies at g * 512 + lane * 16 -- one bulk copy per warp and
-// chunk, and conflict-free 16-byte stores and loads across a warp.
+// q * 32 + lane lies at g * 512 + lane * 16 -- one contiguous 4 KiB block
+// per warp and chunk, and conflict-free 16-byte stores and loads across a warp.
 __device__ __forceinline__ uint32_t splitk_chunk_offset(int c, int q) {
   return static_cast<uint32_t>(c * 4 + q) * 4096u;
 }

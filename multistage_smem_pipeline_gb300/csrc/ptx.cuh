@@ -173,10 +173,6 @@ __device__ __forceinline__ void bulk_wait_group_read() {
   asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 
-__device__ __forceinline__ void bulk_wait_group_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
 // ---------------------------------------------------------------- tcgen05
 // Allocate `ncols` TMEM columns (power of two >= 32); the base address is
 // written to shared memory at `dst`.  Whole warp, converged.
@@ -305,15 +301,6 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
                : "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t cluster_addr,
-                                                              uint32_t bytes) {
-  asm volatile(
-      "mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(
-          cluster_addr),
-      "r"(bytes)
-      : "memory");
-}
-
 // True once the phase with the given parity has completed, with acquire
 // semantics at cluster scope: writes that other CTAs of the cluster made
 // before their release-arrives on this barrier are visible afterwards.
@@ -329,17 +316,6 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
   return ok != 0;
 }
 
-// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from
-// this CTA's shared memory to a shared::cluster address (another CTA's), the
-// bytes completing on an mbarrier given by its shared::cluster address.
-__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster, uint32_t src,
-                                                     uint32_t bytes, uint32_t bar_cluster) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-      ::"r"(dst_cluster), "r"(src), "r"(bytes), "r"(bar_cluster)
-      : "memory");
-}
-
 // 16-byte store into another CTA's shared memory (a shared::cluster address)
 // whose bytes complete on an mbarrier of that CTA (complete_tx), like a bulk
 // copy's: the receiver's wait on the barrier makes the data visible to it.
@@ -350,14 +326,6 @@ __device__ __forceinline__ void st_async_cluster_v4(uint32_t cluster_addr, uint3
           "r"(cluster_addr),
       "r"(a), "r"(b), "r"(c), "r"(d), "r"(bar_cluster)
       : "memory");
-}
-
-// 16-byte store to a shared::cluster address (another CTA's shared memory).
-__device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, uint32_t a, uint32_t b,
-                                              uint32_t c, uint32_t d) {
-  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "r"(a),
-               "r"(b), "r"(c), "r"(d)
-               : "memory");
 }
 
 // TMA load into this CTA's shared memory whose byte count completes on an
